@@ -1,0 +1,514 @@
+// decode.cu -- GQA variable-length sparse decode for sm_103a.
+//
+// Method: TileLang block-sparse Flash-Attention guide, sections 6.1-6.3.  One query token per
+// sequence; the G = Hq/Hkv query heads of kv head g share that head's selected 64-token
+// blocks.  The block_indices slots of each (b, g) are cut into num_splits contiguous slices
+// (section 6.2: the first len % num_splits slices get one extra slot); each slice is one CTA,
+// which writes a partial output and its log-sum-exp, and the partials are merged with
+// weights exp2(lse - max lse) (section 6.1's merge stage).
+//
+// This path is bound by HBM bandwidth (each K/V byte is used once, by G heads), so it is
+// built around bytes in flight: a producer warp streams the K and V tiles of the slice with
+// TMA (128-byte swizzle, two stages of [64 x d] K and V) while four consumer warps each take
+// 16 tokens of every tile.  The [G x 64 x d] products are small, so they run on warp-level
+// mma.sync (G query heads padded to 16 rows) straight out of the swizzled tiles.  The merge
+// is fused: the last CTA of a (b, g) group to finish (atomic ticket) combines the partials
+// and resets the ticket, so a call is a single kernel launch.
+//
+// Differences from the page's kernel: every block that crosses cache_seqlens is masked token
+// by token (the page masks only the first slot and relies on descending order), so the
+// result does not depend on the order of the indices; indices at or past the sequence end
+// are skipped and reported instead of read.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "host_internal.h"
+#include "ptx.cuh"
+
+namespace bsattn {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
+constexpr int kStages = 2;
+constexpr size_t kHeaderBytes = 256;                   // status word + padding
+
+struct DecodeParams {
+    const void* q;
+    const int32_t* seqlens;
+    const int32_t* indices;
+    void* out;
+    int* status;
+    int* tickets;       // [B * Hkv]
+    float* lse_part;    // [B, Hq, ns]
+    float* o_part;      // [B, Hq, ns, d]
+    int B, Hq, Hkv, Smax, max_sel, num_splits;
+    float scale_log2;   // log2(e) / sqrt(d)
+    unsigned long long budget_ns;
+};
+
+template <int D>
+struct DLayout {
+    static constexpr uint32_t kTile = (D / 64) * 8192;      // [64 x D] 16-bit, swizzled halves
+    static constexpr uint32_t kK = 0;
+    static constexpr uint32_t kV = kStages * kTile;
+    static constexpr uint32_t kQ = 2 * kStages * kTile;      // [16 x D] query rows (swizzled)
+    // per-warp partials (m[8], l[8], O[8 x D]) reuse the K/V stages once they are drained
+    static constexpr uint32_t kMerge = 0;
+    static constexpr uint32_t kMergeWarp = (16 + 8 * D) * 4;
+    static constexpr uint32_t kBars = kQ + (D / 64) * 2048;
+    static constexpr uint32_t kMisc = kBars + 8 * 2 * kStages;
+    static constexpr uint32_t kList = kMisc + 16;
+    static uint32_t bytes(int max_slots) { return 1024 + kList + ((4 * max_slots + 15) & ~15); }
+    static_assert(kConsumerWarps * kMergeWarp <= 2 * kStages * kTile, "merge scratch must fit");
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float to_f32(uint16_t raw) {
+    if constexpr (BF16) {
+        return __bfloat162float(__ushort_as_bfloat16(raw));
+    } else {
+        return __half2float(__ushort_as_half(raw));
+    }
+}
+
+// Address (shared-space) of element (row, col) of a swizzled [rows x D] tile stored as D/64
+// column halves of [rows x 64].
+template <int D>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int half_stride, int row, int col) {
+    return base + (col >> 6) * half_stride + sw128_offset(row, col & 63);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeParams p) {
+    using L = DLayout<D>;
+    using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::kBars);
+    uint64_t* empty = full + kStages;
+    int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] count, [1] abort, [2] last
+    int* list = reinterpret_cast<int*>(sm + L::kList);
+    float* merge = reinterpret_cast<float*>(sm + L::kMerge);
+    volatile int* abort_flag = &misc[1];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int G = p.Hq / p.Hkv;
+    const int seqlen = p.seqlens[b];
+    const int nb_valid = (seqlen + 63) / 64;
+    const uint64_t deadline = global_timer_ns() + p.budget_ns;
+
+    // this split's slots (section 6.2 of the guide)
+    const int bps = p.max_sel / p.num_splits, rem = p.max_sel % p.num_splits;
+    const int slot0 = bps * split + min(split, rem);
+    const int nslot = bps + (split < rem ? 1 : 0);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        misc[1] = 0;
+        misc[2] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        // compact the slice: keep 0 <= t < nb_valid; t >= nb_valid is a contract violation
+        const int32_t* slots = p.indices + (static_cast<size_t>(b) * p.Hkv + g) * p.max_sel + slot0;
+        int count = 0;
+        bool bad = false;
+        for (int base = 0; base < nslot; base += 32) {
+            const int j = base + lane;
+            const int t = j < nslot ? slots[j] : -1;
+            const bool on = t >= 0 && t < nb_valid;
+            bad |= t >= nb_valid;
+            const uint32_t ballot = __ballot_sync(0xffffffffu, on);
+            if (on) list[count + __popc(ballot & ((1u << lane) - 1u))] = t;
+            count += __popc(ballot);
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, BSATTN_ERR_BAD_INDEX);
+        if (lane == 0) misc[0] = count;
+    } else if (warp == 1) {
+        // query rows of the group (G <= 8), zero-padded to 16, swizzled like the K tiles
+        const T* qg = reinterpret_cast<const T*>(p.q) + (static_cast<size_t>(b) * p.Hq + g * G) * D;
+        uint8_t* sq = sm + L::kQ;
+        for (int e = lane; e < 16 * D / 8; e += 32) {
+            const int row = e / (D / 8), col = (e % (D / 8)) * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (row < G) v = *reinterpret_cast<const uint4*>(qg + row * D + col);
+            *reinterpret_cast<uint4*>(sq + (col >> 6) * 2048 + sw128_offset(row, col & 63)) = v;
+        }
+    }
+    __syncthreads();
+    const int n = misc[0];
+
+    float o[D / 8][4];                           // consumer state (rows lane/4 < 8 are heads)
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer warp
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            int issued = 0;
+            for (int j = 0; j < n; ++j) {
+                const int st = j % kStages;
+                if (j >= kStages &&
+                    !wait_parity(&empty[st], ((j / kStages) - 1) & 1, deadline, abort_flag, p.status))
+                    break;
+                const int row = b * p.Smax + list[j] * 64;
+                mbar_arrive_expect_tx(&full[st], 2 * kTile);
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d(sm + L::kK + st * kTile + h * 8192, &tm_k, &full[st], h * 64, g, row);
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d(sm + L::kV + st * kTile + h * 8192, &tm_v, &full[st], h * 64, g, row);
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                const uint64_t dl = global_timer_ns() + 200000000ull;
+                for (int j = max(0, issued - kStages); j < issued; ++j)
+                    wait_parity_drain(&full[j % kStages], (j / kStages) & 1, dl);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumer warps 0-3
+        const float c = p.scale_log2;
+        const int tok0 = 16 * warp;                 // this warp's 16 tokens of every tile
+        const uint32_t sq = smem_u32(sm + L::kQ);
+        uint32_t qa[D / 16][4];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int mat = lane >> 3;
+            const int row = (mat & 1) * 8 + (lane & 7);
+            const int col = kk * 16 + (mat >> 1) * 8;
+            ldsm_x4(tile_addr<D>(sq, 2048, row, col), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        for (int j = 0; j < n; ++j) {
+            const int st = j % kStages;
+            if (!warp_wait_parity(&full[st], (j / kStages) & 1, deadline, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            const uint32_t kbase = smem_u32(sm + L::kK + st * kTile);
+            const uint32_t vbase = smem_u32(sm + L::kV + st * kTile);
+            const int key0 = list[j] * 64 + tok0;
+            if (key0 + 16 > seqlen) {
+                // tokens at or past the sequence end may hold anything: zero their V rows so
+                // that P = 0 cannot meet a NaN
+                for (int e = lane; e < 16 * (D / 8); e += 32) {
+                    const int r = e / (D / 8), col = (e % (D / 8)) * 8;
+                    if (key0 + r >= seqlen)
+                        *reinterpret_cast<uint4*>(sm + L::kV + st * kTile + (col >> 6) * 8192 +
+                                                  sw128_offset(tok0 + r, col & 63)) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // S = q K^T over this warp's 16 tokens: two n-tiles of 8 tokens
+            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int mat = lane >> 3;
+                const int tok = tok0 + (mat >> 1) * 8 + (lane & 7);
+                const int col = kk * 16 + (mat & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(tile_addr<D>(kbase, 8192, tok, col), b0, b1, b2, b3);
+                mma16816<BF16>(s[0], qa[kk], b0, b1);
+                mma16816<BF16>(s[1], qa[kk], b2, b3);
+            }
+            // scale to log2 units and mask tokens at or past the sequence end
+            float x[4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = key0 + nt * 8 + 2 * (lane & 3) + e;
+                    x[nt * 2 + e] = key < seqlen ? s[nt][e] * c : -INFINITY;
+                }
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m, mx);
+            const float mref = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = ex2_approx(m - mref);
+            float pr[4], sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                pr[e] = ex2_approx(x[e] - mref);
+                sum += pr[e];
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            l = l * alpha + sum;
+            m = m_new;
+            // P as the A operand (rows 8-15 are padding and stay zero)
+            uint32_t pa[4];
+            pa[0] = pack2<BF16>(pr[0], pr[1]);
+            pa[1] = 0u;
+            pa[2] = pack2<BF16>(pr[2], pr[3]);
+            pa[3] = 0u;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                o[nt][0] *= alpha;
+                o[nt][1] *= alpha;
+            }
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                const int mat = lane >> 3;
+                const int tok = tok0 + (mat & 1) * 8 + (lane & 7);
+                const int col = np * 16 + (mat >> 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(tile_addr<D>(vbase, 8192, tok, col), b0, b1, b2, b3);
+                mma16816<BF16>(o[2 * np], pa, b0, b1);
+                mma16816<BF16>(o[2 * np + 1], pa, b2, b3);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+    }
+    // every warp is done with the K/V stages (and the producer has drained) before they
+    // become merge scratch
+    __syncthreads();
+    if (warp < kConsumerWarps) {
+        // per-warp partial -> shared memory (rows lane/4 < 8 hold the query heads)
+        float* mw = merge + warp * (L::kMergeWarp / 4);
+        if (lane % 4 == 0) {
+            mw[lane / 4] = ok ? m : -INFINITY;
+            mw[8 + lane / 4] = ok ? l : 0.f;
+        }
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            const int col = nt * 8 + 2 * (lane & 3);
+            mw[16 + (lane / 4) * D + col] = o[nt][0];
+            mw[16 + (lane / 4) * D + col + 1] = o[nt][1];
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- combine warps, emit
+    // G rows x D columns, spread over the 128 consumer threads
+    const bool aborted = *abort_flag != 0;
+    const size_t row_base = static_cast<size_t>(b) * p.Hq + g * G;   // first query head row
+    if (tid < 32 * kConsumerWarps) {
+        for (int e = tid; e < G * D; e += 32 * kConsumerWarps) {
+            const int row = e / D, col = e % D;
+            float M = -INFINITY;
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[w * (L::kMergeWarp / 4) + row]);
+            float num = 0.f, den = 0.f;
+            if (M != -INFINITY) {
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float* mw = merge + w * (L::kMergeWarp / 4);
+                    const float wt = ex2_approx(mw[row] - M);
+                    num += wt * mw[16 + row * D + col];
+                    den += wt * mw[8 + row];
+                }
+            }
+            const float val = den > 0.f ? num / den : 0.f;
+            if (p.num_splits == 1) {
+                if (!aborted)
+                    reinterpret_cast<T*>(p.out)[(row_base + row) * D + col] =
+                        BF16 ? T(__float2bfloat16_rn(val)) : T(__float2half_rn(val));
+            } else {
+                const size_t pr = (row_base + row) * p.num_splits + split;
+                p.o_part[pr * D + col] = val;
+                if (col == 0) p.lse_part[pr] = den > 0.f ? M + log2f(den) : -INFINITY;
+            }
+        }
+    }
+    if (p.num_splits == 1) return;
+
+    // last CTA of this (b, g) to arrive merges the num_splits partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int ticket = atomicAdd(&p.tickets[b * p.Hkv + g], 1);
+        misc[2] = ticket == p.num_splits - 1;
+    }
+    __syncthreads();
+    if (!misc[2]) return;
+    __threadfence();
+    for (int e = tid; e < G * D; e += kThreads) {
+        const int row = e / D, col = e % D;
+        const size_t r0 = (row_base + row) * p.num_splits;
+        const volatile float* lse = p.lse_part + r0;
+        const volatile float* op = p.o_part + r0 * D;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < p.num_splits; ++s2) M = fmaxf(M, lse[s2]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+            for (int s2 = 0; s2 < p.num_splits; ++s2) {
+                const float wt = ex2_approx(lse[s2] - M);
+                num += wt * op[s2 * D + col];
+                den += wt;
+            }
+        }
+        const float val = den > 0.f ? num / den : 0.f;
+        reinterpret_cast<T*>(p.out)[(row_base + row) * D + col] =
+            BF16 ? T(__float2bfloat16_rn(val)) : T(__float2half_rn(val));
+    }
+    if (tid == 0) p.tickets[b * p.Hkv + g] = 0;   // ready for the next call
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+    size_t tickets, lse, opart, total;
+};
+
+WsLayout ws_layout(int B, int Hq, int Hkv, int d, int ns) {
+    WsLayout w{};
+    w.tickets = kHeaderBytes;
+    w.lse = w.tickets + align256(sizeof(int) * static_cast<size_t>(B) * Hkv);
+    w.opart = w.lse + align256(sizeof(float) * static_cast<size_t>(B) * Hq * ns);
+    w.total = w.opart + align256(sizeof(float) * static_cast<size_t>(B) * Hq * ns * d);
+    return w;
+}
+
+template <int D, bool BF16>
+int launch(const void* k, const void* v, const DecodeParams& prm, cudaStream_t stream) {
+    CUtensorMap tk, tv;
+    const uint64_t rows = static_cast<uint64_t>(prm.B) * prm.Smax;
+    int rc = 0;
+    rc |= encode_3d(&tk, k, BF16, D, prm.Hkv, rows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
+    rc |= encode_3d(&tv, v, BF16, D, prm.Hkv, rows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
+    if (rc) return rc;
+    const int slots_per_split = (prm.max_sel + prm.num_splits - 1) / prm.num_splits;
+    const uint32_t smem = DLayout<D>::bytes(slots_per_split);
+    if (smem > 227u * 1024u) return BSATTN_ERR_UNSUPPORTED;
+    auto kern = decode_kernel<D, BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return BSATTN_ERR_CUDA;
+    dim3 grid(prm.num_splits, prm.Hkv, prm.B);
+    kern<<<grid, kThreads, smem, stream>>>(tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace bsattn
+
+extern "C" int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int num_sms) {
+    if (num_sms <= 0) num_sms = bsattn::num_sms_of_current_device();
+    if (num_sms <= 0) num_sms = 148;
+    const long long groups = static_cast<long long>(B) * Hkv;
+    if (groups <= 0 || max_sel <= 0) return 1;
+    // about three resident CTAs per SM, each streaming its slice through a 2-stage ring
+    long long s = (3LL * num_sms + groups - 1) / groups;
+    if (s > max_sel) s = max_sel;
+    if (s > 64) s = 64;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+extern "C" size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_sel,
+                                               int num_splits) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return bsattn::kHeaderBytes;
+    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, 0);
+    return bsattn::ws_layout(B, Hq, Hkv, d, ns).total;
+}
+
+extern "C" int bsattn_decode_varlen(const void* q, const void* k, const void* v,
+                                    const int32_t* cache_seqlens, const int32_t* block_indices,
+                                    int num_splits, void* out, int B, int Hq, int Hkv, int Smax,
+                                    int d, int max_sel, bsattn_dtype dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    using namespace bsattn;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Smax < 0 || max_sel < 0 || num_splits < 0)
+        return BSATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv) return BSATTN_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (G > 8) return BSATTN_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return BSATTN_ERR_UNSUPPORTED;
+    if (dtype != BSATTN_F16 && dtype != BSATTN_BF16) return BSATTN_ERR_UNSUPPORTED;
+    if (!workspace) return BSATTN_ERR_INVALID_ARG;
+    if (B == 0) return BSATTN_OK;
+    if (!q || !k || !v || !out || !cache_seqlens || (!block_indices && max_sel > 0))
+        return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return BSATTN_ERR_INVALID_ARG;
+    if (B > 65535 || Hkv > 65535) return BSATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Smax > 0x7fffffffLL) return BSATTN_ERR_UNSUPPORTED;
+    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, 0);
+    if (max_sel == 0) ns = 1;
+    if (ns > max_sel && max_sel > 0) ns = max_sel;
+    const WsLayout w = ws_layout(B, Hq, Hkv, d, ns);
+    if (workspace_bytes < w.total) return BSATTN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (max_sel == 0 || Smax == 0) {
+        return cudaMemsetAsync(out, 0, static_cast<size_t>(B) * Hq * d * 2, st) == cudaSuccess
+                   ? BSATTN_OK
+                   : BSATTN_ERR_CUDA;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeParams prm{};
+    prm.q = q;
+    prm.seqlens = cache_seqlens;
+    prm.indices = block_indices;
+    prm.out = out;
+    prm.status = reinterpret_cast<int*>(ws);
+    prm.tickets = reinterpret_cast<int*>(ws + w.tickets);
+    prm.lse_part = reinterpret_cast<float*>(ws + w.lse);
+    prm.o_part = reinterpret_cast<float*>(ws + w.opart);
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Smax = Smax;
+    prm.max_sel = max_sel;
+    prm.num_splits = ns;
+    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    prm.budget_ns = wait_budget_ns();
+    const bool bf16 = dtype == BSATTN_BF16;
+    if (d == 64) return bf16 ? launch<64, true>(k, v, prm, st) : launch<64, false>(k, v, prm, st);
+    return bf16 ? launch<128, true>(k, v, prm, st) : launch<128, false>(k, v, prm, st);
+}

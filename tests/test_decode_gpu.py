@@ -1,0 +1,145 @@
+"""GPU parity of bsattn_decode_varlen (through the C ABI) against the fp64 oracle.
+
+Tolerance: max |err| <= 2e-2 for bf16 inputs, <= 1e-2 for fp16.  Index handling is exact:
+results must not depend on the order of the indices or on num_splits beyond rounding, a
+selection with no blocks gives exactly 0, tokens past cache_seqlens are never used (they
+hold NaN here), and an index past the sequence end is skipped and flagged.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+TOL = {torch.float16: 1e-2, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module")
+def bsa():
+    import block_sparse_attention_gb300 as m
+    m.load()
+    return m
+
+
+def _run(bsa, q, k, v, sl, idx, ns=0):
+    dev = torch.device("cuda")
+    out = bsa.bsattn_decode_varlen(q.to(dev), k.to(dev), v.to(dev), sl.to(dev),
+                                   idx.to(dev), ns)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def _err(got, want):
+    return float(np.abs(got.double().numpy() - want).max())
+
+
+def _small_case(Hq=8, Hkv=2, d=128, dtype=torch.bfloat16, fill=float("nan")):
+    g = torch.Generator().manual_seed(Hq * 7 + d)
+    B, Smax = 3, 700
+    sl = torch.tensor([700, 1, 333], dtype=torch.int32)
+    q = torch.randn(B, Hq, d, generator=g).to(dtype)
+    k = torch.randn(B, Smax, Hkv, d, generator=g).to(dtype)
+    v = torch.randn(B, Smax, Hkv, d, generator=g).to(dtype)
+    for b in range(B):
+        k[b, sl[b]:] = fill
+        v[b, sl[b]:] = fill
+    idx = torch.full((B, Hkv, 6), -1, dtype=torch.int32)
+    idx[0, 0, :4] = torch.tensor([10, 7, 3, 0])
+    idx[0, -1, :3] = torch.tensor([2, 9, 5])
+    idx[1, 0, :1] = 0
+    idx[2, 0, :2] = torch.tensor([5, 1])
+    idx[2, -1, :6] = torch.tensor([0, 1, 2, 3, 4, 5])
+    return q, k, v, sl, idx
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (8, 1), (16, 8), (6, 3)])
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float16)])
+@pytest.mark.parametrize("ns", [1, 2, 3, 6])
+def test_decode_small_cases(bsa, Hq, Hkv, d, dtype, ns):
+    q, k, v, sl, idx = _small_case(Hq, Hkv, d, dtype)
+    got = _run(bsa, q, k, v, sl, idx, ns)
+    want = oracle.decode_varlen(q, k, v, sl, idx)
+    assert _err(got, want) <= TOL[dtype]
+    zero = np.all(want == 0.0, axis=-1)          # heads whose selection is empty
+    assert np.all(got.double().numpy()[zero] == 0.0)
+    if Hkv > 1:
+        assert zero.any()
+
+
+def test_decode_bad_index_is_skipped_and_flagged(bsa):
+    q, k, v, sl, idx = _small_case()
+    idx[2, 0, 2] = 6            # seqlen 333 -> blocks 0..5 valid; 6 is past the end
+    dev = torch.device("cuda")
+    ws = bsa.workspace(dev, "decode", bsa.bsattn_decode_workspace_size(3, 8, 2, 128, 6, 2))
+    bsa.bsattn_get_device_status(ws)
+    got = _run(bsa, q, k, v, sl, idx, 2)
+    assert bsa.bsattn_get_device_status(ws) & bsa.BSATTN_ERR_BAD_INDEX
+    want = oracle.decode_varlen(q, k, v, sl, idx)
+    assert _err(got, want) <= TOL[torch.bfloat16]
+
+
+@pytest.fixture(scope="module")
+def c5():
+    cfg = synthetic.DECODE_CONFIGS["C5"]
+    q, k, v, sl, idx = synthetic.decode_inputs(cfg, fill=float("nan"))
+    want = oracle.decode_varlen(q, k, v, sl, idx)
+    return cfg, q, k, v, sl, idx, want
+
+
+@pytest.mark.parametrize("ns", [0, 1, 7, 19, 64])
+def test_c5_full_size(bsa, c5, ns):
+    cfg, q, k, v, sl, idx, want = c5
+    got = _run(bsa, q, k, v, sl, idx, ns)
+    assert _err(got, want) <= TOL[cfg.dtype]
+
+
+@pytest.mark.parametrize("order", ["ascending", "shuffled"])
+def test_c5_index_order_does_not_matter(bsa, c5, order):
+    cfg, q, k, v, sl, idx, want = c5
+    if order == "ascending":
+        idx2 = idx.sort(dim=-1).values.contiguous()     # any -1 padding moves to the front
+    else:
+        g = torch.Generator().manual_seed(5)
+        perm = torch.randperm(idx.shape[-1], generator=g)
+        idx2 = idx[..., perm].contiguous()
+    got = _run(bsa, q, k, v, sl, idx2, 0)
+    assert _err(got, want) <= TOL[cfg.dtype]
+
+
+def test_decode_empty_selection_is_zero(bsa, c5):
+    cfg, q, k, v, sl, idx, _ = c5
+    idx2 = idx.clone()
+    idx2[3] = -1
+    got = _run(bsa, q, k, v, sl, idx2, 0)
+    assert torch.count_nonzero(got[3]) == 0
+    want = oracle.decode_varlen(q, k, v, sl, idx2)
+    assert _err(got, want) <= TOL[cfg.dtype]
+
+
+def test_decode_is_deterministic(bsa, c5):
+    cfg, q, k, v, sl, idx, _ = c5
+    assert torch.equal(_run(bsa, q, k, v, sl, idx, 0), _run(bsa, q, k, v, sl, idx, 0))
+
+
+def test_decode_timeout_path_reports_and_recovers(bsa, c5):
+    cfg, q, k, v, sl, idx, want = c5
+    dev = torch.device("cuda")
+    ns = 7
+    ws = torch.zeros(bsa.bsattn_decode_workspace_size(8, 32, 8, 128, 64, ns), dtype=torch.uint8,
+                     device=dev)
+    args = (q.to(dev), k.to(dev), v.to(dev), sl.to(dev), idx.to(dev), ns)
+    try:
+        bsa.bsattn_set_wait_budget_ns(0)
+        bsa.bsattn_decode_varlen(*args, ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        bsa.bsattn_set_wait_budget_ns(2_000_000_000)
+    assert bsa.bsattn_get_device_status(ws) & bsa.BSATTN_ERR_TIMEOUT
+    ws.zero_()
+    got = bsa.bsattn_decode_varlen(*args, ws=ws).cpu()
+    assert bsa.bsattn_get_device_status(ws) == 0
+    assert _err(got, want) <= TOL[cfg.dtype]

@@ -1,0 +1,158 @@
+"""GPU parity of bsattn_prefill (through the C ABI) against the fp64 oracle.
+
+Tolerance (fixed by the task for this method): max |err| <= 1e-2 for fp16 inputs and
+<= 2e-2 for bf16 inputs, both sides fed the same rounded inputs and the same block mask
+(built by the oracle's builder).  Small cases compare every element; the full-size
+workloads compare sampled rows the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+TOL = {torch.float16: 1e-2, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module")
+def bsa():
+    import block_sparse_attention_gb300 as m
+    m.load()
+    return m
+
+
+def _run(bsa, q, k, v, mask, causal):
+    dev = torch.device("cuda")
+    out = bsa.bsattn_prefill(q.to(dev), k.to(dev), v.to(dev), torch.as_tensor(mask).to(dev),
+                             causal)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def _err(got, want):
+    return float(np.abs(got.double().numpy() - want).max()) if want.size else 0.0
+
+
+CASES = [
+    # B, H, Sq, Sk, d, dtype, causal, density
+    (1, 1, 64, 64, 64, torch.float16, True, 1.0),
+    (1, 1, 64, 64, 128, torch.bfloat16, False, 1.0),
+    (1, 2, 130, 130, 64, torch.float16, True, 0.6),
+    (2, 3, 200, 200, 128, torch.bfloat16, True, 0.5),
+    (1, 2, 256, 256, 128, torch.bfloat16, False, 0.5),
+    (1, 1, 1, 1, 64, torch.float16, False, 1.0),
+    (1, 1, 63, 63, 128, torch.bfloat16, True, 1.0),
+    (1, 1, 65, 65, 64, torch.float16, False, 0.7),
+    (2, 2, 512, 512, 64, torch.float16, True, 0.3),
+    (1, 2, 700, 700, 128, torch.bfloat16, True, 0.4),
+    (1, 2, 700, 700, 64, torch.bfloat16, False, 0.25),
+    (1, 1, 1000, 1000, 128, torch.float16, True, 1.0),
+    # Sq != Sk: bottom-right causal alignment, and plain non-causal
+    (1, 2, 100, 300, 64, torch.float16, True, 0.8),
+    (1, 2, 300, 100, 128, torch.bfloat16, True, 0.8),
+    (1, 1, 64, 1000, 128, torch.bfloat16, False, 0.5),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,d,dtype,causal,density", CASES)
+def test_prefill_small_cases(bsa, B, H, Sq, Sk, d, dtype, causal, density):
+    q, k, v = synthetic.qkv(B, H, Sq, Sk, d, dtype, seed=Sq + d)
+    mask = synthetic.random_block_mask(B, H, math.ceil(Sq / 64), math.ceil(Sk / 64), density,
+                                       seed=Sk)
+    got = _run(bsa, q, k, v, mask, causal)
+    want = oracle.prefill(q, k, v, mask, causal)
+    assert _err(got, want) <= TOL[dtype]
+    # rows the oracle says are exactly zero are exactly zero on the GPU too
+    zero_rows = np.all(want == 0.0, axis=-1)
+    assert np.all(got.double().numpy()[zero_rows] == 0.0)
+
+
+def test_prefill_all_masked_is_zero(bsa):
+    q, k, v = synthetic.qkv(1, 2, 300, 300, 128, torch.bfloat16, seed=1)
+    mask = torch.zeros(1, 2, 5, 5, dtype=torch.uint8)
+    got = _run(bsa, q, k, v, mask, True)
+    assert torch.count_nonzero(got) == 0
+
+
+def test_prefill_above_diagonal_entries_ignored_when_causal(bsa):
+    q, k, v = synthetic.qkv(1, 2, 256, 256, 64, torch.float16, seed=2)
+    mask = synthetic.random_block_mask(1, 2, 4, 4, 0.5, seed=2)
+    upper = mask | torch.ones(4, 4, dtype=torch.uint8).triu(1)
+    assert torch.equal(_run(bsa, q, k, v, mask, True), _run(bsa, q, k, v, upper, True))
+
+
+def test_prefill_is_deterministic(bsa):
+    q, k, v = synthetic.qkv(1, 4, 1024, 1024, 128, torch.bfloat16, seed=3)
+    mask = synthetic.random_block_mask(1, 4, 16, 16, 0.5, seed=3)
+    a = _run(bsa, q, k, v, mask, True)
+    b = _run(bsa, q, k, v, mask, True)
+    assert torch.equal(a, b)
+
+
+def test_c1_full_oracle(bsa):
+    cfg = synthetic.PREFILL_CONFIGS["C1"]
+    q, k, v, scores = synthetic.prefill_inputs(cfg)
+    mask = oracle.mask_from_topk(scores, int(cfg.param), cfg.dense_last, cfg.tril)
+    got = _run(bsa, q, k, v, mask, cfg.causal)
+    want = oracle.prefill(q, k, v, mask, cfg.causal)
+    assert _err(got, want) <= TOL[cfg.dtype]
+
+
+def _sampled_rows(nq, S, rng, per_head):
+    rows = {0, S - 1}
+    for qb in rng.choice(nq, size=min(nq, per_head), replace=False):
+        lo = int(qb) * 64
+        hi = min(lo + 64, S)
+        rows |= {lo, hi - 1, int(rng.integers(lo, hi))}
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["C2", "C3", "C4"])
+def test_full_size_workloads_sampled_rows(bsa, name):
+    """The benchmark's workloads at full size, in the benchmark's launch configuration,
+    checked on sampled rows (first/last row of several query blocks per head)."""
+    cfg = synthetic.PREFILL_CONFIGS[name]
+    q, k, v, scores = synthetic.prefill_inputs(cfg)
+    if cfg.rule == "topk":
+        mask = oracle.mask_from_topk(scores, int(cfg.param), cfg.dense_last, cfg.tril)
+    else:
+        mask = oracle.mask_from_threshold(scores, cfg.param, cfg.dense_last, cfg.tril)
+    got = _run(bsa, q, k, v, mask, cfg.causal)
+    rng = np.random.default_rng(0)
+    worst = 0.0
+    for b in range(cfg.B):
+        for h in range(cfg.H):
+            rows = _sampled_rows(cfg.nblk, cfg.S, rng, 3)
+            want = oracle.prefill_rows(q, k, v, mask, cfg.causal, b, h, rows)
+            worst = max(worst, _err(got[b, h, rows], want))
+    assert worst <= TOL[cfg.dtype], worst
+    assert torch.isfinite(got.float()).all()
+
+
+def test_timeout_path_reports_and_recovers(bsa):
+    """A wait budget of 0 makes the kernels' bounded waits expire: the call must record
+    BSATTN_ERR_TIMEOUT in the status word and leave the context usable."""
+    q, k, v = synthetic.qkv(2, 8, 2048, 2048, 128, torch.bfloat16, seed=4)
+    mask = synthetic.random_block_mask(2, 8, 32, 32, 0.5, seed=4)
+    dev = torch.device("cuda")
+    qd, kd, vd, md = q.to(dev), k.to(dev), v.to(dev), mask.to(dev)
+    ws = bsa.workspace(dev, "prefill", 256)
+    bsa.bsattn_get_device_status(ws)            # clear
+    try:
+        bsa.bsattn_set_wait_budget_ns(0)
+        bsa.bsattn_prefill(qd, kd, vd, md, True)
+        torch.cuda.synchronize()
+    finally:
+        bsa.bsattn_set_wait_budget_ns(2_000_000_000)
+    status = bsa.bsattn_get_device_status(ws)
+    assert status & bsa.BSATTN_ERR_TIMEOUT
+    got = bsa.bsattn_prefill(qd, kd, vd, md, True).cpu()
+    assert bsa.bsattn_get_device_status(ws) == 0
+    want = oracle.prefill(q[:1, :2], k[:1, :2], v[:1, :2], mask[:1, :2], True)
+    assert _err(got[:1, :2], want) <= TOL[torch.bfloat16]
