@@ -18,6 +18,7 @@ reported beside it.  L2 is flushed (256 MiB write) before every step, outside th
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -76,10 +77,12 @@ def traffic_record(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms; only the samples whose
+    timestamps fall inside the timed window are summarised."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
@@ -90,7 +93,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -99,9 +102,9 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -110,23 +113,30 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        sm, smax, reasons, power = [], [], set(), []
+        for arrived, ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = arrived
+            if not (t0 <= ts <= t1):
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(self.NAMES, parts[6:10]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(power) if power else None}
 
 
 def dist_setup(args):
@@ -161,11 +171,12 @@ def aggregate(units_per_rank_per_step: float, steps: int, world: int, max_second
 
 # ---------------------------------------------------------------------------- workloads
 
-def build_inputs():
-    import oracle  # mask only: the oracle's builder gives the same mask as the library's
+def build_inputs(mask_builder):
+    """Seeded inputs; the block mask comes from `mask_builder` (the library's host builder
+    on the GPU arm, the oracle's own builder on the CPU arms)."""
     q, k, v, scores = synthetic.prefill_inputs(PREFILL)
-    mask = oracle.mask_from_topk(scores, int(PREFILL.param), PREFILL.dense_last, PREFILL.tril)
-    mask = torch.from_numpy(mask)
+    mask = torch.as_tensor(mask_builder(scores, int(PREFILL.param), PREFILL.dense_last,
+                                        PREFILL.tril))
     dq, dk, dv, sl, idx = synthetic.decode_inputs(DECODE)
     return (q, k, v, mask), (dq, dk, dv, sl, idx)
 
@@ -198,7 +209,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     bsa.load()
-    (q, k, v, mask), (dq, dk, dv, sl, idx) = build_inputs()
+    (q, k, v, mask), (dq, dk, dv, sl, idx) = build_inputs(bsa.bsattn_mask_from_topk)
     flops, pairs = prefill_flops(mask)
     dbytes = decode_bytes(sl, idx)
 
@@ -216,17 +227,19 @@ def run_gpu(args):
         bsa.bsattn_decode_varlen(gdq, gdk, gdv, gsl, gidx, ns, out=dout)
         ev[2].record(stream)
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(args.warmup):
         flush.fill_(1)
         step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
     torch.cuda.synchronize()
+    time.sleep(0.3)            # let the sampler start before the timed window
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    w0 = time.time()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         evs[i][0].record(stream)
@@ -234,7 +247,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t0
-    clk = clocks.stop()
+    clk = clocks.stop(w0, time.time())
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [a + b for a, b in zip(pre_ms, dec_ms)]
@@ -250,7 +263,7 @@ def run_gpu(args):
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
     dq_dev, sl_dev, idx_dev = torch.empty_like(gdq), torch.empty_like(gsl), torch.empty_like(gidx)
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 50))
     h2d_pre = sum(t.numel() * t.element_size() for t in hp)
     h2d_dec = sum(t.numel() * t.element_size() for t in (hdq, hsl, hidx))
     d2h_pre, d2h_dec = hout.numel() * 2, hdout.numel() * 2
@@ -333,7 +346,7 @@ def run_gpu(args):
         "wall_s": round(wall, 3),
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(q, k, v, mask, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(q, k, v, target_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
@@ -375,23 +388,28 @@ def time_oracle_sample(q, k, v, mask, picks):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(q, k, v, mask, target_s=10.0, seed=0):
+def cpu_baseline(q, k, v, target_s=10.0, seed=0):
+    """The oracle, as it stands, on whole 64-row query blocks drawn at random (seeded) from
+    every head of the workload, until `target_s` seconds of CPU work are done."""
+    import numpy as np
     import oracle
     oracle.build()
-    probe = oracle_rows_sample(mask, 64, seed)
-    probe = probe[:2]
-    t = time_oracle_sample(q, k, v, mask, probe)
-    rate = oracle_sample_flops(mask, probe) / max(t, 1e-9)
-    per_head = max(64, int(target_s * rate / (4.0 * 64 * PREFILL.d * 800) / len(mask.flatten(0, 1))
-                          / 64) * 64)
-    per_head = min(per_head, PREFILL.S)
-    picks = oracle_rows_sample(mask, per_head, seed + 1)
-    t = time_oracle_sample(q, k, v, mask, picks)
-    fl = oracle_sample_flops(mask, picks)
-    return {"value": round(fl / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{sum(len(r) for _, _, r in picks)} query rows ({per_head // 64} query "
-                      f"blocks per head, all 16 heads) of the prefill workload, fp64, {t:.1f} s"}
+    _, _, _, scores = synthetic.prefill_inputs(PREFILL)
+    mask = torch.from_numpy(oracle.mask_from_topk(scores, int(PREFILL.param), PREFILL.dense_last,
+                                                  PREFILL.tril))
+    rng = np.random.default_rng(seed)
+    B, H, nq, _ = mask.shape
+    t_total, flops, blocks = 0.0, 0.0, 0
+    while t_total < target_s:
+        b, h, qb = int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(nq))
+        picks = [(b, h, list(range(qb * 64, min(qb * 64 + 64, PREFILL.S))))]
+        t_total += time_oracle_sample(q, k, v, mask, picks)
+        flops += oracle_sample_flops(mask, picks)
+        blocks += 1
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{blocks} random 64-row query blocks ({blocks * 64} rows) of the prefill "
+                      f"workload, fp64, {t_total:.1f} s of oracle time"}
 
 
 def run_reference(args):
@@ -400,7 +418,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    (q, k, v, mask), _ = build_inputs()
+    (q, k, v, mask), _ = build_inputs(oracle.mask_from_topk)
     # each step: one query block per head, drawn afresh (a bounded sample of the workload)
     for i in range(args.warmup):
         time_oracle_sample(q, k, v, mask, oracle_rows_sample(mask, 64, 1000 + i))
@@ -428,8 +446,8 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["bsattn", "reference"], default="bsattn")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
