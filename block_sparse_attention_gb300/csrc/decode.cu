@@ -23,6 +23,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <mutex>
 #include <type_traits>
 
 #include "host_internal.h"
@@ -511,4 +512,65 @@ extern "C" int bsattn_decode_varlen(const void* q, const void* k, const void* v,
     const bool bf16 = dtype == BSATTN_BF16;
     if (d == 64) return bf16 ? launch<64, true>(k, v, prm, st) : launch<64, false>(k, v, prm, st);
     return bf16 ? launch<128, true>(k, v, prm, st) : launch<128, false>(k, v, prm, st);
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// Some callers cannot allocate device memory at the point where they attend: code running
+// inside a custom allocator or memory pool (which must not re-enter it), a runtime that
+// pre-plans every buffer and forbids allocation after start-up, or a host integration
+// that only ever hands over pointers to buffers it already owns.  For them the scratch the
+// decode needs (split partials, LSE values, merge tickets) lives in the fixed array below,
+// part of the library's own image: every GPU that loads the library holds it until exit.
+
+namespace bsattn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The host-side symbol is only
+// a stand-in, so the address is looked up once per device with that device current.
+int noalloc_scratch(void** ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return BSATTN_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return BSATTN_OK;
+}
+
+}  // namespace
+}  // namespace bsattn
+
+extern "C" int bsattn_decode_varlen_noalloc(const void* q, const void* k, const void* v,
+                                            const int32_t* cache_seqlens,
+                                            const int32_t* block_indices, int num_splits,
+                                            void* out, int B, int Hq, int Hkv, int Smax, int d,
+                                            int max_sel, bsattn_dtype dtype, void* stream) {
+    using namespace bsattn;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_sel < 0 || num_splits < 0) return BSATTN_ERR_INVALID_ARG;
+    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, 0);
+    if (max_sel == 0) ns = 1;
+    if (ns > max_sel && max_sel > 0) ns = max_sel;
+    const size_t need = bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, ns);
+    if (need > kNoAllocScratchBytes) return BSATTN_ERR_UNSUPPORTED;   // shape beyond the array
+    void* scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    // the array keeps the previous call's contents: the status word and the merge tickets
+    // must start at zero
+    const WsLayout w = ws_layout(B > 0 ? B : 1, Hq, Hkv, d, ns);
+    if (cudaMemsetAsync(scratch, 0, w.lse, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BSATTN_ERR_CUDA;
+    return bsattn_decode_varlen(q, k, v, cache_seqlens, block_indices, ns, out, B, Hq, Hkv, Smax,
+                                d, max_sel, dtype, scratch, kNoAllocScratchBytes, stream);
 }

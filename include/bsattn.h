@@ -104,6 +104,29 @@ int bsattn_decode_varlen(const void* q, const void* k, const void* v,
                          int max_sel, bsattn_dtype dtype, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/*
+ * bsattn_decode_varlen without a workspace argument, for callers that cannot allocate
+ * device memory when they attend (code running inside a custom allocator or memory pool,
+ * runtimes that forbid allocation after start-up, hosts that only pass pointers to buffers
+ * they own).  The pages have no counterpart: this is a deployment variant of the decode
+ * above, with the same arguments (minus the workspace) and the same results.
+ *
+ * Its scratch is one fixed 8 MiB device array inside the library (held by every GPU that
+ * loads the library until the process exits); shapes whose decode workspace
+ * (bsattn_decode_workspace_size) exceeds it return BSATTN_ERR_UNSUPPORTED.  It allocates
+ * nothing: no cudaMalloc / cudaFree, no allocating library routine.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Each call clears the array's
+ * status word and merge tickets with cudaMemsetAsync on `stream`.  All calls share the
+ * array, so calls that overlap on the GPU (different streams, or threads) race and must be
+ * serialised by the caller.  Device-detected conditions (a skipped out-of-range index, an
+ * expired wait) are not reported by this variant.
+ */
+int bsattn_decode_varlen_noalloc(const void* q, const void* k, const void* v,
+                                 const int32_t* cache_seqlens, const int32_t* block_indices,
+                                 int num_splits, void* out, int B, int Hq, int Hkv, int Smax,
+                                 int d, int max_sel, bsattn_dtype dtype, void* stream);
+
 /* Workspace bytes bsattn_decode_varlen needs (num_splits 0 = the library's choice). */
 size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_sel, int num_splits);
 
