@@ -219,7 +219,7 @@ def run_gpu(args):
     dout = torch.empty_like(gdq)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ns = bsa.bsattn_decode_default_splits(DECODE.B, DECODE.Hkv, DECODE.max_sel, 0)
+    ns = bsa.bsattn_decode_default_splits(DECODE.B, DECODE.Hkv, DECODE.max_sel, DECODE.d)
 
     def step(ev):
         bsa.bsattn_prefill(gq, gk, gv, gm, True, out=out)

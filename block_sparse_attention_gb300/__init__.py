@@ -72,7 +72,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 "bsattn_prefill_workspace_size": ([I, I, I, I], Z),
                 "bsattn_decode_varlen": ([P, P, P, P, P, I, P, I, I, I, I, I, I, I, P, Z, P], I),
                 "bsattn_decode_workspace_size": ([I, I, I, I, I, I], Z),
-                "bsattn_decode_default_splits": ([I, I, I, I], I),
+                "bsattn_decode_default_splits": ([I, I, I, I, I], I),
                 "bsattn_num_splits_heuristic": ([I, I, I, I, ctypes.c_longlong, I, I], I),
                 "bsattn_mask_from_topk": ([P, I, I, I, I, I, I, I, P], I),
                 "bsattn_mask_from_threshold": ([P, I, I, I, I, ctypes.c_float, I, I, P], I),
@@ -170,8 +170,9 @@ def bsattn_prefill(q, k, v, block_mask, is_causal: bool, out=None, ws=None):
     return out
 
 
-def bsattn_decode_default_splits(B: int, Hkv: int, max_sel: int, num_sms: int = 0) -> int:
-    return int(load().bsattn_decode_default_splits(B, Hkv, max_sel, num_sms))
+def bsattn_decode_default_splits(B: int, Hkv: int, max_sel: int, d: int = 128,
+                                 num_sms: int = 0) -> int:
+    return int(load().bsattn_decode_default_splits(B, Hkv, max_sel, d, num_sms))
 
 
 def bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, num_splits=0) -> int:

@@ -441,13 +441,40 @@ int launch(const void* k, const void* v, const DecodeParams& prm, cudaStream_t s
 }  // namespace
 }  // namespace bsattn
 
-extern "C" int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int num_sms) {
+namespace bsattn {
+namespace {
+
+// Resident decode CTAs per SM for head dim d (smem sized for a slice of max_sel slots).
+int decode_ctas_per_sm(int d, int max_sel) {
+    int occ = 0;
+    cudaError_t e;
+    if (d == 64) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<64, true>, kThreads,
+                                                          DLayout<64>::bytes(max_sel));
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<128, true>, kThreads,
+                                                          DLayout<128>::bytes(max_sel));
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return occ;
+}
+
+}  // namespace
+}  // namespace bsattn
+
+extern "C" int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int d, int num_sms) {
     if (num_sms <= 0) num_sms = bsattn::num_sms_of_current_device();
     if (num_sms <= 0) num_sms = 148;
     const long long groups = static_cast<long long>(B) * Hkv;
     if (groups <= 0 || max_sel <= 0) return 1;
-    // about three resident CTAs per SM, each streaming its slice through a 2-stage ring
-    long long s = (3LL * num_sms + groups - 1) / groups;
+    int per_sm = (d == 64 || d == 128) ? bsattn::decode_ctas_per_sm(d, max_sel) : 0;
+    if (per_sm <= 0) per_sm = 3;
+    // as many splits as fill exactly one wave of resident CTAs: every CTA streams its
+    // slice from the start, and no second, mostly empty wave follows
+    long long s = static_cast<long long>(per_sm) * num_sms / groups;
     if (s > max_sel) s = max_sel;
     if (s > 64) s = 64;
     return s < 1 ? 1 : static_cast<int>(s);
@@ -456,7 +483,7 @@ extern "C" int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int num
 extern "C" size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_sel,
                                                int num_splits) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return bsattn::kHeaderBytes;
-    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, 0);
+    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, d, 0);
     return bsattn::ws_layout(B, Hq, Hkv, d, ns).total;
 }
 
@@ -480,7 +507,7 @@ extern "C" int bsattn_decode_varlen(const void* q, const void* k, const void* v,
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return BSATTN_ERR_INVALID_ARG;
     if (B > 65535 || Hkv > 65535) return BSATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(B) * Smax > 0x7fffffffLL) return BSATTN_ERR_UNSUPPORTED;
-    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, 0);
+    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, d, 0);
     if (max_sel == 0) ns = 1;
     if (ns > max_sel && max_sel > 0) ns = max_sel;
     const WsLayout w = ws_layout(B, Hq, Hkv, d, ns);
@@ -558,7 +585,7 @@ extern "C" int bsattn_decode_varlen_noalloc(const void* q, const void* k, const 
                                             int max_sel, bsattn_dtype dtype, void* stream) {
     using namespace bsattn;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || max_sel < 0 || num_splits < 0) return BSATTN_ERR_INVALID_ARG;
-    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, 0);
+    int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, d, 0);
     if (max_sel == 0) ns = 1;
     if (ns > max_sel && max_sel > 0) ns = max_sel;
     const size_t need = bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, ns);

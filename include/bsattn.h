@@ -131,11 +131,12 @@ int bsattn_decode_varlen_noalloc(const void* q, const void* k, const void* v,
 size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_sel, int num_splits);
 
 /*
- * The split count bsattn_decode_varlen uses when num_splits == 0: enough CTAs to keep
- * every SM streaming K/V from HBM (the decode is bandwidth-bound), capped by max_sel.
- * num_sms <= 0 queries the current device.
+ * The split count bsattn_decode_varlen uses when num_splits == 0: the decode is bound by HBM
+ * bandwidth, so it takes as many splits as fill exactly one wave of resident CTAs (resident
+ * CTAs per SM for head dim d x num_sms, divided over the B * Hkv groups), capped by max_sel
+ * and 64.  num_sms <= 0 queries the current device.
  */
-int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int num_sms);
+int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int d, int num_sms);
 
 /*
  * The split-count rule of [BSA] 6.3, bit-exact: if total_mblocks >= 0.8 num_SMs return 1
