@@ -458,12 +458,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             if (!inB) s[4 * rep + 2 + e] = -INFINITY;
                         }
                 }
-                float mx[2] = {-INFINITY, -INFINITY};
+                // row maxima as trees (rows A and B interleave in s[4 rep + 0..1 / 2..3])
+                float t8[8];
 #pragma unroll
-                for (int rep = 0; rep < 8; ++rep) {
-                    mx[0] = fmaxf(mx[0], fmaxf(s[4 * rep], s[4 * rep + 1]));
-                    mx[1] = fmaxf(mx[1], fmaxf(s[4 * rep + 2], s[4 * rep + 3]));
+                for (int rep = 0; rep < 4; ++rep) {
+                    t8[rep] = fmaxf(fmaxf(s[8 * rep], s[8 * rep + 1]), fmaxf(s[8 * rep + 4], s[8 * rep + 5]));
+                    t8[4 + rep] = fmaxf(fmaxf(s[8 * rep + 2], s[8 * rep + 3]), fmaxf(s[8 * rep + 6], s[8 * rep + 7]));
                 }
+                float mx[2] = {fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                               fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7]))};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
@@ -480,16 +483,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     m_used[h] = m_new;
                     mc[h] = m_new == -INFINITY ? 0.f : m_new * c;
                 }
-                float sum[2] = {0.f, 0.f};
 #pragma unroll
                 for (int rep = 0; rep < 8; ++rep) {
                     s[4 * rep + 0] = ex2_approx(fmaf(s[4 * rep + 0], c, -mc[0]));
                     s[4 * rep + 1] = ex2_approx(fmaf(s[4 * rep + 1], c, -mc[0]));
                     s[4 * rep + 2] = ex2_approx(fmaf(s[4 * rep + 2], c, -mc[1]));
                     s[4 * rep + 3] = ex2_approx(fmaf(s[4 * rep + 3], c, -mc[1]));
-                    sum[0] += s[4 * rep + 0] + s[4 * rep + 1];
-                    sum[1] += s[4 * rep + 2] + s[4 * rep + 3];
                 }
+#pragma unroll
+                for (int rep = 0; rep < 4; ++rep) {
+                    t8[rep] = (s[8 * rep] + s[8 * rep + 1]) + (s[8 * rep + 4] + s[8 * rep + 5]);
+                    t8[4 + rep] = (s[8 * rep + 2] + s[8 * rep + 3]) + (s[8 * rep + 6] + s[8 * rep + 7]);
+                }
+                float sum[2] = {(t8[0] + t8[1]) + (t8[2] + t8[3]), (t8[4] + t8[5]) + (t8[6] + t8[7])};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
@@ -519,13 +525,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                     tmem_wait_st();
                 }
+                // P -> the swizzled P tile: matrix (row group, 8-column group); lane 8i + r
+                // addresses row r of matrix i of each x4 store
 #pragma unroll
-                for (int rep = 0; rep < 8; ++rep) {
-                    const int col = 8 * rep + 2 * qi;
-                    *reinterpret_cast<uint32_t*>(sp + sw128_offset(lrowA, col)) =
-                        pack2<BF16>(s[4 * rep + 0], s[4 * rep + 1]);
-                    *reinterpret_cast<uint32_t*>(sp + sw128_offset(lrowB, col)) =
-                        pack2<BF16>(s[4 * rep + 2], s[4 * rep + 3]);
+                for (int j = 0; j < 4; ++j) {
+                    const int mi = lane >> 3, rr = lane & 7;
+                    const int row = 16 * warp + (mi & 1) * 8 + rr;
+                    const int chunk = (2 * j + (mi >> 1)) ^ rr;
+                    stsm_x4(smem_u32(sp) + row * 128 + chunk * 16,
+                            pack2<BF16>(s[8 * j + 0], s[8 * j + 1]), pack2<BF16>(s[8 * j + 2], s[8 * j + 3]),
+                            pack2<BF16>(s[8 * j + 4], s[8 * j + 5]), pack2<BF16>(s[8 * j + 6], s[8 * j + 7]));
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();

@@ -249,6 +249,16 @@ __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_
         : "memory");
 }
 
+// Four 8x8 16-bit matrices from registers to shared memory: lanes 8i..8i+7 give the row
+// addresses (16 bytes each) of matrix i; register i of lane t holds row t/4, columns
+// 2(t%4), 2(t%4)+1 of matrix i (the layout of an mma / tcgen05 16x256b accumulator).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading / stride
