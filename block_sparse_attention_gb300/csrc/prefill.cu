@@ -60,14 +60,29 @@ constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by 
 constexpr int kCtasPerSm = 2;
 constexpr int kSlots = 3;               // items published ahead of the consumers
 
-// workspace words (int): status, work counter, finished-CTA counter
+// workspace words (int): status, work counter, finished-CTA counter, continuation queue head,
+// partial-slot counter, call epoch; then the continuation entries, the per-row merge tickets,
+// the partial LSE values and the partial outputs of rows split across CTAs
 constexpr int kWsStatus = 0;
 constexpr int kWsNext = 16;
 constexpr int kWsDone = 32;
+constexpr int kWsContHead = 48;
+constexpr int kWsPoolNext = 49;
+constexpr int kWsEpoch = 50;
+constexpr size_t kWsHeaderBytes = 1024;
+constexpr int kMaxSlots = 2048;         // partial outputs that can be in use at once
+constexpr int kSplitMin = 96;           // rows visiting more key blocks than this are split
+constexpr int kSplitLen = 64;           // ... into parts of this many blocks
+constexpr int kSplitMinNk = 1024;       // splitting is on only when rows can be this long
+constexpr int kEntryInts = 8;           // t, start, len, part, nparts, slot base, ready, -
 
 struct PrefillParams {
     const uint8_t* mask;
     int* ws;                            // status word + scheduler counters
+    int* entries;                       // [kMaxSlots][kEntryInts]; nullptr: no splitting
+    int* tickets;                       // [kMaxSlots]
+    float* lse;                         // [kMaxSlots][64]
+    float* opart;                       // [kMaxSlots][64][d]
     void* out;
     int B, H, Sq, Sk, nq, nk;
     int causal;
@@ -85,10 +100,10 @@ struct Layout {
     static constexpr uint32_t kP = kV + kVStages * kTile; // one [64 x 64] P tile
     static constexpr uint32_t kBars = kP + 8192;
     // q_full q_free k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] s_free[2]
-    // p_full o_done o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded
-    static constexpr uint32_t kNumBars = 2 + 2 * kKStages + 2 * kVStages + 4 + 3 + 2 * kSlots + 3;
-    static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, item[slots], cnt[slots]
-    static constexpr uint32_t kList = kMisc + 16 + 8 * kSlots;
+    // p_full o_done o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
+    static constexpr uint32_t kNumBars = 2 + 2 * kKStages + 2 * kVStages + 4 + 3 + 2 * kSlots + 5;
+    static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
+    static constexpr uint32_t kList = kMisc + 16 + 20 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
     static uint32_t bytes(int nk) { return 1024 + kList + kSlots * list_stride(nk); }
 };
@@ -142,9 +157,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* fin_s = item_empty + kSlots;
     uint64_t* fin_pv = fin_s + 1;
     uint64_t* loaded = fin_pv + 1;                 // the producer has issued an item's loads
+    uint64_t* pdone = loaded + 1;                  // softmax warps wrote a split part's partial
+    uint64_t* mdec = pdone + 1;                    // merge decision of a split row is known
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] tmem [1] abort [2..] item, count
     int* item_of = misc + 4;                             // [slots]
-    int* count_of = item_of + kSlots;                    // [slots]
+    int* count_of = item_of + kSlots;                    // [slots] blocks of this (part of a) row
+    int* part_of = count_of + kSlots;                    // [slots]
+    int* nparts_of = part_of + kSlots;                   // [slots] 1 = row not split
+    int* sbase_of = nparts_of + kSlots;                  // [slots] first partial slot of the row
+    int* merge_flag = sbase_of + kSlots;                 // [1]
     const uint32_t lstride = L::list_stride(p.nk);
     uint16_t* lists = reinterpret_cast<uint16_t*>(sm + L::kList);
     volatile int* abort_flag = &misc[1];
@@ -180,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(fin_s, 1);
         mbar_init(fin_pv, 1);
         mbar_init(loaded, 1);
+        mbar_init(pdone, 4);
+        mbar_init(mdec, 1);
         misc[1] = 0;
         fence_barrier_init();
     }
@@ -194,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     if (warp == kSchedWarp) {
         // ------------------------------------------------------------ scheduler warp
+        const int epoch = p.ws[kWsEpoch];
+        volatile int* vws = p.ws;
         for (int n = 0;; ++n) {
             const int slot = n % kSlots;
             // take item n only once the producer has issued every load of item n-1: a CTA then
@@ -203,9 +228,60 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (n >= kSlots && !warp_wait_parity(&item_empty[slot], ((n / kSlots) - 1) & 1, deadline,
                                                  abort_flag, status))
                 break;
-            int t = 0;
-            if (lane == 0) t = atomicAdd(p.ws + kWsNext, 1);
-            t = __shfl_sync(0xffffffffu, t, 0);
+            // 1. a continuation part of a long row split by another CTA, if one is queued; once
+            //    the work counter is exhausted the queue is drained before this CTA stops
+            auto claim = [&]() -> int {
+                int e = -1;
+                if (lane == 0 && p.entries) {
+                    for (;;) {
+                        const int h = vws[kWsContHead];
+                        const int tl = min(vws[kWsPoolNext], kMaxSlots);
+                        if (h >= tl) break;
+                        if (atomicCAS(p.ws + kWsContHead, h, h + 1) != h) continue;
+                        volatile int* ent = p.entries + h * kEntryInts;
+                        // the entry is written right after its slot is reserved
+                        uint32_t spins = 0;
+                        bool ready;
+                        while (!(ready = ent[6] == epoch + 1)) {
+                            if ((spins++ & 63u) == 0 && global_timer_ns() > deadline) {
+                                atomicOr(status, BSATTN_ERR_TIMEOUT);
+                                *abort_flag = 1;
+                                break;
+                            }
+                        }
+                        if (!ready) break;
+                        __threadfence();
+                        if (ent[4] > 0) {   // a part to run (first-part entries are markers)
+                            e = h;
+                            break;
+                        }
+                    }
+                }
+                return __shfl_sync(0xffffffffu, e, 0);
+            };
+            int e = claim();
+            if (*abort_flag) break;
+            int t, start = 0, len = 0x7fffffff, part = 0, nparts = 1, sbase = -1;
+            if (e < 0) {
+                t = 0;
+                if (lane == 0) t = atomicAdd(p.ws + kWsNext, 1);
+                t = __shfl_sync(0xffffffffu, t, 0);
+                if (t >= p.total_items) {
+                    // no fresh rows left: parts other CTAs queued may still arrive until every
+                    // CTA has taken its last row, and queued parts are always run by someone
+                    e = claim();
+                    if (*abort_flag) break;
+                }
+            }
+            if (e >= 0) {
+                volatile int* ent = p.entries + e * kEntryInts;
+                t = ent[0];
+                start = ent[1];
+                len = ent[2];
+                part = ent[3];
+                nparts = ent[4];
+                sbase = ent[5];
+            }
             if (t >= p.total_items) {
                 if (lane == 0) {
                     item_of[slot] = -1;
@@ -221,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const long long lim = last_key / 64 + 1;
                 kb_end = last_key < 0 ? 0 : (lim < p.nk ? static_cast<int>(lim) : p.nk);
             }
-            // compact the mask row: visited key blocks in ascending order
+            // 2. compact the mask row (visited key blocks in ascending order) into the slot's
+            //    list, keeping entries [start, start + len) of it
             const uint8_t* mrow = p.mask + (static_cast<size_t>(bh) * p.nq + qb) * p.nk;
             uint16_t* list = lists + slot * (lstride / 2);
             int count = 0;
@@ -229,13 +306,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int kb = base + lane;
                 const bool on = kb < kb_end && mrow[kb] != 0;
                 const uint32_t ballot = __ballot_sync(0xffffffffu, on);
-                if (on) list[count + __popc(ballot & ((1u << lane) - 1u))] = static_cast<uint16_t>(kb);
+                const int pos = count + __popc(ballot & ((1u << lane) - 1u)) - start;
+                if (on && pos >= 0 && pos < len) list[pos] = static_cast<uint16_t>(kb);
                 count += __popc(ballot);
+            }
+            // 3. a fresh row that visits many key blocks is split: this CTA keeps the first
+            //    part, the others are queued for any CTA to take
+            if (e < 0 && p.entries && count > kSplitMin) {
+                const int np = (count + kSplitLen - 1) / kSplitLen;
+                int base_slot = 0;
+                if (lane == 0) base_slot = atomicAdd(p.ws + kWsPoolNext, np);
+                base_slot = __shfl_sync(0xffffffffu, base_slot, 0);
+                const bool fits = base_slot + np <= kMaxSlots;     // else: the pool is full
+                for (int i = lane; i < np && base_slot + i < kMaxSlots; i += 32) {
+                    int* ent = p.entries + (base_slot + i) * kEntryInts;
+                    const int st = i * kSplitLen;
+                    ent[0] = t;
+                    ent[1] = st;
+                    ent[2] = min(kSplitLen, count - st);
+                    ent[3] = i;
+                    ent[4] = (i == 0 || !fits) ? 0 : np;        // markers are skipped by claimers
+                    ent[5] = base_slot;
+                    __threadfence();
+                    reinterpret_cast<volatile int*>(ent)[6] = epoch + 1;
+                }
+                if (fits) {
+                    nparts = np;
+                    sbase = base_slot;
+                    len = kSplitLen;
+                }
             }
             __syncwarp();
             if (lane == 0) {
                 item_of[slot] = t;
-                count_of[slot] = count;
+                count_of[slot] = min(count - start, len);
+                part_of[slot] = part;
+                nparts_of[slot] = nparts;
+                sbase_of[slot] = sbase;
                 mbar_arrive(&item_full[slot]);   // release: the list is visible to the waiters
             }
         }
@@ -401,13 +508,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int lrowB = lrowA + 8;
         const uint32_t tl = tbase + (static_cast<uint32_t>(32 * warp) << 16);
         const float c = p.scale_log2;
-        int blk = 0, qloads = 0;
+        int blk = 0, qloads = 0, nsplit = 0;
         for (int n = 0;; ++n) {
             const int slot = n % kSlots;
             if (!warp_wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
             const int item = item_of[slot];
             const int cnt = count_of[slot];
             if (item < 0) break;
+            const int part = part_of[slot], nparts = nparts_of[slot], sbase = sbase_of[slot];
             int bh, qb;
             decode_item(item, BH, p.nq, bh, qb);
             const uint16_t* list = lists + slot * (lstride / 2);
@@ -546,48 +654,140 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (!warp_wait_parity(o_done, glast & 1, deadline, abort_flag, status)) break;
             tc_fence_after();
             const float inv[2] = {l[0] > 0.f ? 1.f / l[0] : 0.f, l[1] > 0.f ? 1.f / l[1] : 0.f};
-            uint32_t ob[D / 2];
+            if (nparts > 1) {
+                // one part of a row split across CTAs: its O / l (fp32) and log2-sum-exp go to the
+                // row's partial slots; the last part to finish merges them with LSE weights
+                float* op = p.opart + static_cast<size_t>(sbase + part) * 64 * D;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t o[16];
-                tmem_ld_16x256b_x4(tl + kOCol + c0, o);
-                tmem_wait_ld();
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[16];
+                    tmem_ld_16x256b_x4(tl + kOCol + c0, o);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int rep = 0; rep < 4; ++rep) {
-                    ob[c0 / 4 + rep] = pack2<BF16>(__uint_as_float(o[4 * rep + 0]) * inv[0],
-                                                   __uint_as_float(o[4 * rep + 1]) * inv[0]);
-                    ob[c0 / 4 + 4 + rep] = pack2<BF16>(__uint_as_float(o[4 * rep + 2]) * inv[1],
-                                                       __uint_as_float(o[4 * rep + 3]) * inv[1]);
-                }
-            }
-            // O is in registers: the next item's first P V may overwrite it
-            tc_fence_before();
-            mbar_arrive(o_free);
-            // Within a quad, thread j holds column pair 2j of each 8-column group; a 4-step
-            // exchange gives thread qi the whole group qi of its rows: one 16-byte store each.
-            T* orow = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + qb * 64) * D;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t* src = ob + c0 / 4 + 4 * h;
-                    uint32_t g0 = 0, g1 = 0, g2 = 0, g3 = 0;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int want = (qi + r) & 3;          // group the reader of this lane needs
-                        const uint32_t send = want == 0 ? src[0] : want == 1 ? src[1] : want == 2 ? src[2] : src[3];
-                        const int from = (qi - r) & 3;          // its pair sits at column 8 qi + 2 from
-                        const uint32_t got = __shfl_sync(0xffffffffu, send, (lane & ~3) | from);
-                        g0 = from == 0 ? got : g0;
-                        g1 = from == 1 ? got : g1;
-                        g2 = from == 2 ? got : g2;
-                        g3 = from == 3 ? got : g3;
+                    for (int rep = 0; rep < 4; ++rep) {
+                        const int col = c0 + 8 * rep + 2 * qi;
+                        *reinterpret_cast<float2*>(op + lrowA * D + col) =
+                            make_float2(__uint_as_float(o[4 * rep + 0]) * inv[0], __uint_as_float(o[4 * rep + 1]) * inv[0]);
+                        *reinterpret_cast<float2*>(op + lrowB * D + col) =
+                            make_float2(__uint_as_float(o[4 * rep + 2]) * inv[1], __uint_as_float(o[4 * rep + 3]) * inv[1]);
                     }
-                    const int row = h == 0 ? lrowA : lrowB;
-                    if (qb * 64 + row < p.Sq)
-                        *reinterpret_cast<uint4*>(orow + static_cast<size_t>(row) * D + c0 + 8 * qi) =
-                            make_uint4(g0, g1, g2, g3);
                 }
+                tc_fence_before();
+                mbar_arrive(o_free);
+                if (qi == 0) {
+                    float* lp = p.lse + static_cast<size_t>(sbase + part) * 64;
+                    lp[lrowA] = l[0] > 0.f ? m_used[0] * c + log2f(l[0]) : -INFINITY;
+                    lp[lrowB] = l[1] > 0.f ? m_used[1] * c + log2f(l[1]) : -INFINITY;
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pdone);
+                if (tid == 0) {
+                    int last = 0;
+                    if (wait_parity(pdone, nsplit & 1, deadline, abort_flag, status)) {
+                        last = atomicAdd(p.tickets + sbase, 1) == nparts - 1;
+                        if (last) p.tickets[sbase] = 0;   // ready for the next call
+                    }
+                    *merge_flag = last;
+                    mbar_arrive(mdec);
+                }
+                if (!warp_wait_parity(mdec, nsplit & 1, deadline, abort_flag, status)) break;
+                ++nsplit;
+                if (*reinterpret_cast<volatile int*>(merge_flag)) {
+                    __threadfence();
+                    // row-wise merge: warp w takes rows 16w..16w+15; per row the part weights
+                    // are computed once and each lane streams D/32 columns of every part
+                    T* orow = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + qb * 64) * D;
+                    const float* lsr = p.lse + static_cast<size_t>(sbase) * 64;
+                    const float* opr = p.opart + static_cast<size_t>(sbase) * 64 * D;
+                    constexpr int kCols = D / 32;                 // 2 (d=64) or 4 (d=128)
+                    for (int rr = 0; rr < 16; ++rr) {
+                        const int r = 16 * warp + rr;
+                        if (qb * 64 + r >= p.Sq) break;
+                        float lp = -INFINITY;
+                        if (lane < nparts) lp = __ldcg(lsr + lane * 64 + r);
+                        float M = lp;
+#pragma unroll
+                        for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+                        const float w = (M == -INFINITY || lane >= nparts) ? 0.f : ex2_approx(lp - M);
+                        float den = w;
+#pragma unroll
+                        for (int x = 16; x >= 1; x >>= 1) den += __shfl_xor_sync(0xffffffffu, den, x);
+                        float acc[kCols];
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
+                        for (int pp = 0; pp < nparts; ++pp) {
+                            const float wp = __shfl_sync(0xffffffffu, w, pp & 31);
+                            const float* src = opr + static_cast<size_t>(pp) * 64 * D + r * D + lane * kCols;
+                            if constexpr (kCols == 4) {
+                                const float4 v4 = __ldcg(reinterpret_cast<const float4*>(src));
+                                acc[0] += wp * v4.x;
+                                acc[1] += wp * v4.y;
+                                acc[2] += wp * v4.z;
+                                acc[3] += wp * v4.w;
+                            } else {
+                                const float2 v2 = __ldcg(reinterpret_cast<const float2*>(src));
+                                acc[0] += wp * v2.x;
+                                acc[1] += wp * v2.y;
+                            }
+                        }
+                        const float invd = den > 0.f ? 1.f / den : 0.f;
+                        uint32_t packed[kCols / 2];
+#pragma unroll
+                        for (int j = 0; j < kCols / 2; ++j)
+                            packed[j] = pack2<BF16>(acc[2 * j] * invd, acc[2 * j + 1] * invd);
+                        T* dst = orow + static_cast<size_t>(r) * D + lane * kCols;
+                        if constexpr (kCols == 4) {
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+                        } else {
+                            *reinterpret_cast<uint32_t*>(dst) = packed[0];
+                        }
+                    }
+                }
+            } else {
+                uint32_t ob[D / 2];
+    #pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[16];
+                    tmem_ld_16x256b_x4(tl + kOCol + c0, o);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int rep = 0; rep < 4; ++rep) {
+                        ob[c0 / 4 + rep] = pack2<BF16>(__uint_as_float(o[4 * rep + 0]) * inv[0],
+                                                       __uint_as_float(o[4 * rep + 1]) * inv[0]);
+                        ob[c0 / 4 + 4 + rep] = pack2<BF16>(__uint_as_float(o[4 * rep + 2]) * inv[1],
+                                                           __uint_as_float(o[4 * rep + 3]) * inv[1]);
+                    }
+                }
+                // O is in registers: the next item's first P V may overwrite it
+                tc_fence_before();
+                mbar_arrive(o_free);
+                // Within a quad, thread j holds column pair 2j of each 8-column group; a 4-step
+                // exchange gives thread qi the whole group qi of its rows: one 16-byte store each.
+                T* orow = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + qb * 64) * D;
+    #pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32)
+    #pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t* src = ob + c0 / 4 + 4 * h;
+                        uint32_t g0 = 0, g1 = 0, g2 = 0, g3 = 0;
+    #pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int want = (qi + r) & 3;          // group the reader of this lane needs
+                            const uint32_t send = want == 0 ? src[0] : want == 1 ? src[1] : want == 2 ? src[2] : src[3];
+                            const int from = (qi - r) & 3;          // its pair sits at column 8 qi + 2 from
+                            const uint32_t got = __shfl_sync(0xffffffffu, send, (lane & ~3) | from);
+                            g0 = from == 0 ? got : g0;
+                            g1 = from == 1 ? got : g1;
+                            g2 = from == 2 ? got : g2;
+                            g3 = from == 3 ? got : g3;
+                        }
+                        const int row = h == 0 ? lrowA : lrowB;
+                        if (qb * 64 + row < p.Sq)
+                            *reinterpret_cast<uint4*>(orow + static_cast<size_t>(row) * D + c0 + 8 * qi) =
+                                make_uint4(g0, g1, g2, g3);
+                    }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             blk += cnt;
@@ -607,6 +807,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int done = atomicAdd(p.ws + kWsDone, 1);
         if (done == static_cast<int>(gridDim.x) - 1) {
             atomicExch(p.ws + kWsNext, 0);
+            atomicExch(p.ws + kWsContHead, 0);
+            atomicExch(p.ws + kWsPoolNext, 0);
+            atomicAdd(p.ws + kWsEpoch, 1);       // queue entries of this call are now stale
             atomicExch(p.ws + kWsDone, 0);
         }
     }
@@ -640,7 +843,19 @@ int launch(const void* q, const void* k, const void* v, const PrefillParams& prm
 }  // namespace
 }  // namespace bsattn
 
-extern "C" size_t bsattn_prefill_workspace_size(int, int, int, int) { return 256; }
+namespace bsattn {
+namespace {
+// bytes of each workspace region (partial outputs sized for d = 128)
+constexpr size_t kWsEntriesOff = kWsHeaderBytes;
+constexpr size_t kWsTicketsOff = kWsEntriesOff + sizeof(int) * kMaxSlots * kEntryInts;
+constexpr size_t kWsLseOff = kWsTicketsOff + sizeof(int) * kMaxSlots;
+constexpr size_t kWsOpartOff = kWsLseOff + sizeof(float) * kMaxSlots * 64;
+constexpr size_t kWsFullBytes = kWsOpartOff + sizeof(float) * kMaxSlots * 64 * 128;
+constexpr size_t kWsMinBytes = 256;
+}  // namespace
+}  // namespace bsattn
+
+extern "C" size_t bsattn_prefill_workspace_size(int, int, int, int) { return bsattn::kWsFullBytes; }
 
 extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
                               int is_causal, void* out, int B, int H, int Sq, int Sk, int d,
@@ -650,8 +865,7 @@ extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const
     if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return BSATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return BSATTN_ERR_UNSUPPORTED;
     if (dtype != BSATTN_F16 && dtype != BSATTN_BF16) return BSATTN_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < bsattn_prefill_workspace_size(B, H, Sq, Sk))
-        return BSATTN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kWsMinBytes) return BSATTN_ERR_INVALID_ARG;
     const long long BH = static_cast<long long>(B) * H;
     if (BH == 0 || Sq == 0) return BSATTN_OK;
     if (!q || !k || !v || !out || !block_mask) return BSATTN_ERR_INVALID_ARG;
@@ -669,6 +883,15 @@ extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const
     PrefillParams prm{};
     prm.mask = block_mask;
     prm.ws = static_cast<int*>(workspace);
+    if (workspace_bytes >= kWsFullBytes && nk >= kSplitMinNk) {
+        // room for the continuation queue and partial outputs, and rows long enough that one
+        // of them could outlast the rest of the launch: long rows are split
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        prm.entries = reinterpret_cast<int*>(w + kWsEntriesOff);
+        prm.tickets = reinterpret_cast<int*>(w + kWsTicketsOff);
+        prm.lse = reinterpret_cast<float*>(w + kWsLseOff);
+        prm.opart = reinterpret_cast<float*>(w + kWsOpartOff);
+    }
     prm.out = out;
     prm.B = B;
     prm.H = H;

@@ -66,14 +66,19 @@ const char* bsattn_version(void);
  *   k, v        (device) [B, H, Sk, d]  dtype
  *   block_mask  (device) [B, H, ceil(Sq/64), ceil(Sk/64)] uint8, nonzero = visit
  *   out         (device) [B, H, Sq, d]  dtype, fully written (rows with no work = 0)
- *   workspace   (device) >= bsattn_prefill_workspace_size() bytes, zero-filled once
+ *   workspace   (device) >= 256 bytes, zero-filled once, 16-byte aligned: scheduler counters
+ *               and the status word.  With bsattn_prefill_workspace_size() bytes (64 MiB) and
+ *               rows that can span 1024+ key blocks, a row visiting more than 96 key blocks is
+ *               split into 64-block parts run by different CTAs and merged by log-sum-exp
+ *               (2048 partial slots; rows that do not fit run whole, so results are
+ *               bit-reproducible only while the slots suffice).
  * q, k, v, out must be 16-byte aligned.  Returns BSATTN_OK or an error status.
  */
 int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
                    int is_causal, void* out, int B, int H, int Sq, int Sk, int d,
                    bsattn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes bsattn_prefill needs for this shape. */
+/* Workspace bytes that enable splitting long rows (256 bytes is the minimum). */
 size_t bsattn_prefill_workspace_size(int B, int H, int Sq, int Sk);
 
 /*

@@ -156,3 +156,29 @@ def test_timeout_path_reports_and_recovers(bsa):
     assert bsa.bsattn_get_device_status(ws) == 0
     want = oracle.prefill(q[:1, :2], k[:1, :2], v[:1, :2], mask[:1, :2], True)
     assert _err(got[:1, :2], want) <= TOL[torch.bfloat16]
+
+
+def test_long_rows_split_across_ctas(bsa):
+    """Rows visiting more than 96 key blocks are split into parts run by different CTAs and
+    merged by log-sum-exp once rows can span 1024+ key blocks (64K+ keys); the result matches
+    the oracle, matches an unsplit run (minimal workspace) within rounding, and is the same
+    from run to run."""
+    dev = torch.device("cuda")
+    B, H, S, d = 1, 2, 66000, 128
+    q, k, v = synthetic.qkv(B, H, S, S, d, torch.bfloat16, seed=21)
+    nb = math.ceil(S / 64)
+    # 5% of the blocks, plus the last two query-block rows dense (1031 and 1032 blocks): only
+    # those rows are split (17 parts each), well within the 2048 partial slots
+    mask = synthetic.random_block_mask(B, H, nb, nb, 0.05, seed=21)
+    mask[:, :, -2:, :] = 1
+    args = [t.to(dev) for t in (q, k, v, mask)]
+    split = bsa.bsattn_prefill(*args, True).cpu()
+    again = bsa.bsattn_prefill(*args, True).cpu()
+    assert torch.equal(split, again)
+    small_ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    whole = bsa.bsattn_prefill(*args, True, ws=small_ws).cpu()
+    assert float((split.float() - whole.float()).abs().max()) <= 2e-2
+    rows = [0, 63, 6100, 40000, 65535, 65920, 65990, 65999]
+    for h in range(H):
+        want = oracle.prefill_rows(q, k, v, mask, True, 0, h, rows)
+        assert _err(split[0, h, rows], want) <= TOL[torch.bfloat16]
