@@ -29,6 +29,7 @@ __all__ = [
     "bsattn_decode_workspace_size", "bsattn_decode_default_splits", "bsattn_num_splits_heuristic",
     "bsattn_mask_from_topk", "bsattn_mask_from_threshold", "bsattn_get_device_status",
     "bsattn_set_wait_budget_ns", "bsattn_status_string", "bsattn_version", "workspace",
+    "bsattn_decode_varlen_mask", "bsattn_decode_paged", "bsattn_mask_from_cumulative_threshold",
 ]
 
 BSATTN_OK = 0
@@ -77,6 +78,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 "bsattn_mask_from_topk": ([P, I, I, I, I, I, I, I, P], I),
                 "bsattn_mask_from_threshold": ([P, I, I, I, I, ctypes.c_float, I, I, P], I),
                 "bsattn_get_device_status": ([P, P], I),
+                "bsattn_decode_varlen_mask": ([P, P, P, P, P, I, P, I, I, I, I, I, I, I, P, Z, P], I),
+                "bsattn_decode_paged": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, I, P, Z, P], I),
+                "bsattn_mask_from_cumulative_threshold": ([P, I, I, I, I, ctypes.c_double, I, P], I),
                 "bsattn_set_wait_budget_ns": ([ctypes.c_ulonglong], None),
             }
             for name, (args, res) in sig.items():
@@ -204,6 +208,74 @@ def bsattn_decode_varlen(q, k, v, cache_seqlens, block_indices, num_splits: int 
                                   int(num_splits), out.data_ptr(), B, Hq, Hkv, Smax, d, max_sel,
                                   _dtype_code(q), ws.data_ptr(), ws.numel(), _stream(q.device))
     _check("bsattn_decode_varlen", rc)
+    return out
+
+
+def bsattn_decode_varlen_mask(q, k, v, cache_seqlens, block_mask, num_splits: int = 0, out=None,
+                              ws=None):
+    """GQA varlen sparse decode, block-mask form.  block_mask [B,Hkv,num_blocks] uint8/bool."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("cache_seqlens", cache_seqlens),
+                    ("block_mask", block_mask)):
+        _cuda_contig(name, t)
+    if block_mask.dtype == torch.bool:
+        block_mask = block_mask.view(torch.uint8)
+    if cache_seqlens.dtype != torch.int32 or block_mask.dtype != torch.uint8:
+        raise TypeError("cache_seqlens must be int32 and block_mask uint8/bool")
+    B, Hq, d = q.shape
+    _, Smax, Hkv, _ = k.shape
+    nb = block_mask.shape[2]
+    if tuple(block_mask.shape[:2]) != (B, Hkv) or k.shape != v.shape:
+        raise ValueError("decode shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(q.device, "decode", bsattn_decode_workspace_size(B, Hq, Hkv, d, nb, num_splits))
+    rc = lib.bsattn_decode_varlen_mask(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       cache_seqlens.data_ptr(), block_mask.data_ptr(),
+                                       int(num_splits), out.data_ptr(), B, Hq, Hkv, Smax, d, nb,
+                                       _dtype_code(q), ws.data_ptr(), ws.numel(), _stream(q.device))
+    _check("bsattn_decode_varlen_mask", rc)
+    return out
+
+
+def bsattn_decode_paged(q, k_pages, v_pages, cache_seqlens, block_indices, block_table,
+                        num_splits: int = 0, out=None, ws=None):
+    """GQA varlen sparse decode over a paged KV cache.  k_pages/v_pages
+    [num_pages, page_size, Hkv, d]; block_table int32 [B, max_pages_per_seq]."""
+    lib = load()
+    for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
+                    ("cache_seqlens", cache_seqlens), ("block_indices", block_indices),
+                    ("block_table", block_table)):
+        _cuda_contig(name, t)
+    if (cache_seqlens.dtype, block_indices.dtype, block_table.dtype) != (torch.int32,) * 3:
+        raise TypeError("cache_seqlens, block_indices and block_table must be int32")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    max_sel = block_indices.shape[2]
+    if k_pages.shape != v_pages.shape or tuple(block_indices.shape[:2]) != (B, Hkv):
+        raise ValueError("paged decode shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(q.device, "decode", bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, num_splits))
+    rc = lib.bsattn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                 cache_seqlens.data_ptr(), block_indices.data_ptr(),
+                                 block_table.data_ptr(), int(num_splits), out.data_ptr(), B, Hq,
+                                 Hkv, num_pages, page_size, block_table.shape[1], d, max_sel,
+                                 _dtype_code(q), ws.data_ptr(), ws.numel(), _stream(q.device))
+    _check("bsattn_decode_paged", rc)
+    return out
+
+
+def bsattn_mask_from_cumulative_threshold(attn_sum, threshold: float, causal: bool = True):
+    """Host-side XAttention cumulative-threshold block mask; CPU uint8 tensor."""
+    s = _host_scores(attn_sum)
+    B, H, nq, nk = s.shape
+    out = torch.empty(s.shape, dtype=torch.uint8)
+    rc = load().bsattn_mask_from_cumulative_threshold(s.data_ptr(), B, H, nq, nk, float(threshold),
+                                                      int(bool(causal)), out.data_ptr())
+    _check("bsattn_mask_from_cumulative_threshold", rc)
     return out
 
 

@@ -37,10 +37,21 @@ constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
 constexpr int kStages = 2;
 constexpr size_t kHeaderBytes = 256;                   // status word + padding
 
+// Where a CTA's key blocks come from (all give the same token set semantics):
+//   kIndices  block_indices [B, Hkv, max_sel] int32, contiguous cache [B, Smax, Hkv, d]
+//   kMask     block_mask [B, Hkv, max_sel] uint8 (slot j <-> block j), contiguous cache
+//   kPaged    block_indices as kIndices; K/V in pages [num_pages, page_size, Hkv, d] reached
+//             through block_table [B, max_pages] (guide section 7)
+enum DecodeMode { kIndices = 0, kMask = 1, kPaged = 2 };
+
 struct DecodeParams {
     const void* q;
     const int32_t* seqlens;
     const int32_t* indices;
+    const uint8_t* mask;
+    const int32_t* block_table;
+    int mode;
+    int page_size, max_pages, num_pages;
     void* out;
     int* status;
     int* tickets;       // [B * Hkv]
@@ -63,7 +74,8 @@ struct DLayout {
     static constexpr uint32_t kBars = kQ + (D / 64) * 2048;
     static constexpr uint32_t kMisc = kBars + 8 * 2 * kStages;
     static constexpr uint32_t kList = kMisc + 16;
-    static uint32_t bytes(int max_slots) { return 1024 + kList + ((4 * max_slots + 15) & ~15); }
+    // two int lists per slot: logical block (sequence-end masking) and TMA row of its tile
+    static uint32_t bytes(int max_slots) { return 1024 + kList + 2 * ((4 * max_slots + 15) & ~15); }
     static_assert(kConsumerWarps * kMergeWarp <= 2 * kStages * kTile, "merge scratch must fit");
 };
 
@@ -127,7 +139,7 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int half_stride, in
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeParams p) {
     using L = DLayout<D>;
@@ -140,6 +152,8 @@ __global__ void __launch_bounds__(kThreads)
     uint64_t* empty = full + kStages;
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] count, [1] abort, [2] last
     int* list = reinterpret_cast<int*>(sm + L::kList);
+    const int slot_cap = (p.max_sel + p.num_splits - 1) / p.num_splits;
+    int* rows = list + ((4 * slot_cap + 15) & ~15) / 4;
     float* merge = reinterpret_cast<float*>(sm + L::kMerge);
     volatile int* abort_flag = &misc[1];
 
@@ -165,17 +179,45 @@ __global__ void __launch_bounds__(kThreads)
         fence_barrier_init();
     }
     if (warp == 0) {
-        // compact the slice: keep 0 <= t < nb_valid; t >= nb_valid is a contract violation
-        const int32_t* slots = p.indices + (static_cast<size_t>(b) * p.Hkv + g) * p.max_sel + slot0;
+        // compact the slice: keep blocks 0 <= t < nb_valid and resolve the TMA row of each
+        const size_t sel_off = (static_cast<size_t>(b) * p.Hkv + g) * p.max_sel + slot0;
         int count = 0;
         bool bad = false;
         for (int base = 0; base < nslot; base += 32) {
             const int j = base + lane;
-            const int t = j < nslot ? slots[j] : -1;
-            const bool on = t >= 0 && t < nb_valid;
-            bad |= t >= nb_valid;
+            int t = -1;
+            if (j < nslot) {
+                if (p.mode == kMask) {
+                    t = p.mask[sel_off + j] ? slot0 + j : -1;   // mask slots past the end: ignored
+                    if (t >= nb_valid) t = -1;
+                } else {
+                    t = p.indices[sel_off + j];
+                }
+            }
+            bool on = t >= 0 && t < nb_valid;
+            bad |= t >= nb_valid;                               // an index past the sequence end
+            int row = 0;
+            if (on) {
+                if (p.mode == kPaged) {
+                    const long long pos = static_cast<long long>(t) * 64;
+                    const long long lp = pos / p.page_size;
+                    const int page = lp < p.max_pages ? p.block_table[static_cast<size_t>(b) * p.max_pages + lp] : -1;
+                    if (page < 0 || page >= p.num_pages) {
+                        on = false;                             // unmapped page: skip, flag
+                        bad = true;
+                    } else {
+                        row = page * p.page_size + static_cast<int>(pos - lp * p.page_size);
+                    }
+                } else {
+                    row = b * p.Smax + t * 64;
+                }
+            }
             const uint32_t ballot = __ballot_sync(0xffffffffu, on);
-            if (on) list[count + __popc(ballot & ((1u << lane) - 1u))] = t;
+            if (on) {
+                const int pos = count + __popc(ballot & ((1u << lane) - 1u));
+                list[pos] = t;
+                rows[pos] = row;
+            }
             count += __popc(ballot);
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, BSATTN_ERR_BAD_INDEX);
@@ -208,7 +250,7 @@ __global__ void __launch_bounds__(kThreads)
                 if (j >= kStages &&
                     !wait_parity(&empty[st], ((j / kStages) - 1) & 1, deadline, abort_flag, p.status))
                     break;
-                const int row = b * p.Smax + list[j] * 64;
+                const int row = rows[j];
                 mbar_arrive_expect_tx(&full[st], 2 * kTile);
                 for (int h = 0; h < D / 64; ++h)
                     tma_load_3d(sm + L::kK + st * kTile + h * 8192, &tm_k, &full[st], h * 64, g, row);
@@ -422,10 +464,12 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int d, int ns) {
 template <int D, bool BF16>
 int launch(const void* k, const void* v, const DecodeParams& prm, cudaStream_t stream) {
     CUtensorMap tk, tv;
-    const uint64_t rows = static_cast<uint64_t>(prm.B) * prm.Smax;
+    // rows of the K/V tensors as TMA sees them: B * Smax tokens, or num_pages * page_size
+    const uint64_t nrows = prm.mode == kPaged ? static_cast<uint64_t>(prm.num_pages) * prm.page_size
+                                              : static_cast<uint64_t>(prm.B) * prm.Smax;
     int rc = 0;
-    rc |= encode_3d(&tk, k, BF16, D, prm.Hkv, rows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
-    rc |= encode_3d(&tv, v, BF16, D, prm.Hkv, rows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
+    rc |= encode_3d(&tk, k, BF16, D, prm.Hkv, nrows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
+    rc |= encode_3d(&tv, v, BF16, D, prm.Hkv, nrows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
     if (rc) return rc;
     const int slots_per_split = (prm.max_sel + prm.num_splits - 1) / prm.num_splits;
     const uint32_t smem = DLayout<D>::bytes(slots_per_split);
@@ -487,58 +531,123 @@ extern "C" size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, in
     return bsattn::ws_layout(B, Hq, Hkv, d, ns).total;
 }
 
-extern "C" int bsattn_decode_varlen(const void* q, const void* k, const void* v,
-                                    const int32_t* cache_seqlens, const int32_t* block_indices,
-                                    int num_splits, void* out, int B, int Hq, int Hkv, int Smax,
-                                    int d, int max_sel, bsattn_dtype dtype, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
-    using namespace bsattn;
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Smax < 0 || max_sel < 0 || num_splits < 0)
-        return BSATTN_ERR_INVALID_ARG;
+namespace bsattn {
+namespace {
+
+// Shared body of the decode entry points: argument checks, split count, workspace carving.
+int decode_impl(DecodeParams prm, const void* k, const void* v, int num_splits, int d,
+                bsattn_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+    const int B = prm.B, Hq = prm.Hq, Hkv = prm.Hkv, max_sel = prm.max_sel;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_sel < 0 || num_splits < 0) return BSATTN_ERR_INVALID_ARG;
     if (Hq % Hkv) return BSATTN_ERR_INVALID_ARG;
-    const int G = Hq / Hkv;
-    if (G > 8) return BSATTN_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 8) return BSATTN_ERR_UNSUPPORTED;
     if (d != 64 && d != 128) return BSATTN_ERR_UNSUPPORTED;
     if (dtype != BSATTN_F16 && dtype != BSATTN_BF16) return BSATTN_ERR_UNSUPPORTED;
     if (!workspace) return BSATTN_ERR_INVALID_ARG;
     if (B == 0) return BSATTN_OK;
-    if (!q || !k || !v || !out || !cache_seqlens || (!block_indices && max_sel > 0))
+    const bool sel_ok = prm.mode == kMask ? prm.mask != nullptr : prm.indices != nullptr;
+    if (!prm.q || !k || !v || !prm.out || !prm.seqlens || (!sel_ok && max_sel > 0) ||
+        (prm.mode == kPaged && !prm.block_table))
         return BSATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(prm.q) || !aligned16(k) || !aligned16(v) || !aligned16(prm.out)) return BSATTN_ERR_INVALID_ARG;
     if (B > 65535 || Hkv > 65535) return BSATTN_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * Smax > 0x7fffffffLL) return BSATTN_ERR_UNSUPPORTED;
+    if (prm.mode == kPaged) {
+        if (prm.page_size <= 0 || prm.page_size % 64 || prm.num_pages <= 0 || prm.max_pages <= 0)
+            return prm.page_size > 0 && prm.page_size % 64 ? BSATTN_ERR_UNSUPPORTED : BSATTN_ERR_INVALID_ARG;
+        if (static_cast<long long>(prm.num_pages) * prm.page_size > 0x7fffffffLL) return BSATTN_ERR_UNSUPPORTED;
+    } else {
+        if (prm.Smax < 0) return BSATTN_ERR_INVALID_ARG;
+        if (static_cast<long long>(B) * prm.Smax > 0x7fffffffLL) return BSATTN_ERR_UNSUPPORTED;
+    }
     int ns = num_splits > 0 ? num_splits : bsattn_decode_default_splits(B, Hkv, max_sel, d, 0);
     if (max_sel == 0) ns = 1;
     if (ns > max_sel && max_sel > 0) ns = max_sel;
     const WsLayout w = ws_layout(B, Hq, Hkv, d, ns);
     if (workspace_bytes < w.total) return BSATTN_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (max_sel == 0 || Smax == 0) {
-        return cudaMemsetAsync(out, 0, static_cast<size_t>(B) * Hq * d * 2, st) == cudaSuccess
+    if (max_sel == 0 || (prm.mode != kPaged && prm.Smax == 0)) {
+        return cudaMemsetAsync(prm.out, 0, static_cast<size_t>(B) * Hq * d * 2, st) == cudaSuccess
                    ? BSATTN_OK
                    : BSATTN_ERR_CUDA;
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    DecodeParams prm{};
-    prm.q = q;
-    prm.seqlens = cache_seqlens;
-    prm.indices = block_indices;
-    prm.out = out;
     prm.status = reinterpret_cast<int*>(ws);
     prm.tickets = reinterpret_cast<int*>(ws + w.tickets);
     prm.lse_part = reinterpret_cast<float*>(ws + w.lse);
     prm.o_part = reinterpret_cast<float*>(ws + w.opart);
-    prm.B = B;
-    prm.Hq = Hq;
-    prm.Hkv = Hkv;
-    prm.Smax = Smax;
-    prm.max_sel = max_sel;
     prm.num_splits = ns;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.budget_ns = wait_budget_ns();
     const bool bf16 = dtype == BSATTN_BF16;
     if (d == 64) return bf16 ? launch<64, true>(k, v, prm, st) : launch<64, false>(k, v, prm, st);
     return bf16 ? launch<128, true>(k, v, prm, st) : launch<128, false>(k, v, prm, st);
+}
+
+}  // namespace
+}  // namespace bsattn
+
+extern "C" int bsattn_decode_varlen(const void* q, const void* k, const void* v,
+                                    const int32_t* cache_seqlens, const int32_t* block_indices,
+                                    int num_splits, void* out, int B, int Hq, int Hkv, int Smax,
+                                    int d, int max_sel, bsattn_dtype dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    bsattn::DecodeParams prm{};
+    prm.q = q;
+    prm.seqlens = cache_seqlens;
+    prm.indices = block_indices;
+    prm.mode = bsattn::kIndices;
+    prm.out = out;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Smax = Smax;
+    prm.max_sel = max_sel;
+    return bsattn::decode_impl(prm, k, v, num_splits, d, dtype, workspace, workspace_bytes,
+                               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int bsattn_decode_varlen_mask(const void* q, const void* k, const void* v,
+                                         const int32_t* cache_seqlens, const uint8_t* block_mask,
+                                         int num_splits, void* out, int B, int Hq, int Hkv,
+                                         int Smax, int d, int num_blocks, bsattn_dtype dtype,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+    bsattn::DecodeParams prm{};
+    prm.q = q;
+    prm.seqlens = cache_seqlens;
+    prm.mask = block_mask;
+    prm.mode = bsattn::kMask;
+    prm.out = out;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Smax = Smax;
+    prm.max_sel = num_blocks;
+    return bsattn::decode_impl(prm, k, v, num_splits, d, dtype, workspace, workspace_bytes,
+                               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int bsattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                   const int32_t* cache_seqlens, const int32_t* block_indices,
+                                   const int32_t* block_table, int num_splits, void* out, int B,
+                                   int Hq, int Hkv, int num_pages, int page_size,
+                                   int max_pages_per_seq, int d, int max_sel, bsattn_dtype dtype,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    bsattn::DecodeParams prm{};
+    prm.q = q;
+    prm.seqlens = cache_seqlens;
+    prm.indices = block_indices;
+    prm.block_table = block_table;
+    prm.mode = bsattn::kPaged;
+    prm.page_size = page_size;
+    prm.max_pages = max_pages_per_seq;
+    prm.num_pages = num_pages;
+    prm.out = out;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Smax = 0;
+    prm.max_sel = max_sel;
+    return bsattn::decode_impl(prm, k_pages, v_pages, num_splits, d, dtype, workspace,
+                               workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- allocation-free variant

@@ -160,6 +160,37 @@ int bsattn_mask_from_threshold(const float* scores, int B, int H, int nq, int nk
     return BSATTN_OK;
 }
 
+int bsattn_mask_from_cumulative_threshold(const float* attn_sum, int B, int H, int nq, int nk,
+                                          double threshold, int causal, uint8_t* mask_out) {
+    int rc = check_scores(attn_sum, B, H, nq, nk, mask_out);
+    if (rc) return rc;
+    std::vector<int> order;
+    order.reserve(static_cast<size_t>(nk));
+    for (long long r = 0; r < static_cast<long long>(B) * H * nq; ++r) {
+        const int i = static_cast<int>(r % nq);
+        const float* row = attn_sum + static_cast<size_t>(r) * nk;
+        uint8_t* m = mask_out + static_cast<size_t>(r) * nk;
+        std::memset(m, 0, nk);
+        if (nk == 0) continue;
+        double total = 0.0;
+        for (int j = 0; j < nk; ++j) total += static_cast<double>(row[j]);
+        m[0] = 1;                                   // the sink block
+        if (causal && i < nk) m[i] = 1;             // the diagonal block
+        order.clear();
+        for (int j = 0; j < nk; ++j)
+            if (!m[j]) order.push_back(j);
+        std::stable_sort(order.begin(), order.end(), [row](int a, int b) { return row[a] > row[b]; });
+        const double required = total * threshold;
+        double acc = 0.0;
+        for (int j : order) {
+            if (acc >= required) break;
+            m[j] = 1;
+            acc += static_cast<double>(row[j]);
+        }
+    }
+    return BSATTN_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------- TMA descriptor encoding

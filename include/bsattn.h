@@ -8,6 +8,8 @@
  *         split heuristic, 7 paged KV decode.
  *   [FA]  "使用 TileLang 实现 FlashAttention ... 完整实战指南" (TileLang FlashAttention
  *         guide): online softmax, bottom-right causal alignment when seq_kv > seq_q.
+ *   [XA]  "XAttention 算法实现指南" (XAttention algorithm guide): block selection
+ *         (find_blocks_chunked) and its worked example.
  *
  * Conventions for every call:
  *   - Pointers marked (device) are caller-owned device memory; (host) caller-owned host
@@ -132,6 +134,37 @@ int bsattn_decode_varlen_noalloc(const void* q, const void* k, const void* v,
                                  int num_splits, void* out, int B, int Hq, int Hkv, int Smax,
                                  int d, int max_sel, bsattn_dtype dtype, void* stream);
 
+/*
+ * GQA varlen sparse decode, block-mask form -- [BSA] 6 (the `_mask` example).  Identical to
+ * bsattn_decode_varlen except that the selected blocks of (b, g) are given as
+ *   block_mask (device) [B, Hkv, num_blocks] uint8, nonzero = block j selected;
+ * slot j of the mask is block j, and the num_blocks slots are cut into num_splits slices as in
+ * [BSA] 6.2.  Set entries at or past the sequence end select no tokens (not flagged).
+ * Workspace: bsattn_decode_workspace_size(B, Hq, Hkv, d, num_blocks, num_splits) bytes.
+ */
+int bsattn_decode_varlen_mask(const void* q, const void* k, const void* v,
+                              const int32_t* cache_seqlens, const uint8_t* block_mask,
+                              int num_splits, void* out, int B, int Hq, int Hkv, int Smax, int d,
+                              int num_blocks, bsattn_dtype dtype, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * GQA varlen sparse decode over a paged KV cache -- [BSA] 7.  As bsattn_decode_varlen, but
+ *   k_pages, v_pages (device) [num_pages, page_size, Hkv, d] dtype
+ *   block_table      (device) [B, max_pages_per_seq] int32: logical page p of sequence b is
+ *                    physical page block_table[b][p]
+ * Logical token position P of sequence b lives in page block_table[b][P / page_size], row
+ * P % page_size.  page_size must be a multiple of 64 (a 64-token block never straddles two
+ * pages; [BSA] 7 asserts the same).  Blocks whose page is out of range are skipped and flagged
+ * BSATTN_ERR_BAD_INDEX.  Workspace as for bsattn_decode_varlen.
+ */
+int bsattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* cache_seqlens, const int32_t* block_indices,
+                        const int32_t* block_table, int num_splits, void* out, int B, int Hq,
+                        int Hkv, int num_pages, int page_size, int max_pages_per_seq, int d,
+                        int max_sel, bsattn_dtype dtype, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* Workspace bytes bsattn_decode_varlen needs (num_splits 0 = the library's choice). */
 size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_sel, int num_splits);
 
@@ -168,6 +201,18 @@ int bsattn_mask_from_topk(const float* scores, int B, int H, int nq, int nk, int
 int bsattn_mask_from_threshold(const float* scores, int B, int H, int nq, int nk,
                                float threshold, int use_dense_for_last_block, int apply_tril,
                                uint8_t* mask_out);
+
+/*
+ * Cumulative-threshold block mask -- [XA] "block selection (find_blocks_chunked)".  attn_sum
+ * (host) fp32 [B, H, nq, nk] holds per (query block, key block) attention weight sums.  Per
+ * row: block 0 (the sink) is kept and, when causal, the diagonal block i (if i < nk); the other
+ * blocks are visited from the largest weight down (ties: lower column first) and taken while
+ * the sum of the weights already taken is below threshold * (row total), so the block whose
+ * addition reaches the threshold is taken too.  Sums are in double, left to right.
+ * mask_out (host) uint8 [B, H, nq, nk].  NaN weights -> BSATTN_ERR_INVALID_ARG.
+ */
+int bsattn_mask_from_cumulative_threshold(const float* attn_sum, int B, int H, int nq, int nk,
+                                          double threshold, int causal, uint8_t* mask_out);
 
 /*
  * Reads and clears the device status word at the start of `workspace` (device), after

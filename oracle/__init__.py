@@ -347,7 +347,10 @@ def find_blocks_chunked(attn_sum, threshold: float, causal: bool = True) -> np.n
                 mask[b, h, i, 0] = 1
                 if causal and i < nk:
                     mask[b, h, i, i] = 1
+                total = 0.0
+                for val in row:                  # the row total, summed left to right
+                    total += float(val)
                 rest = {j: float(row[j]) for j in range(nk) if not mask[b, h, i, j]}
-                for j in cumulative_pick(rest, float(row.sum()) * threshold):
+                for j in cumulative_pick(rest, total * threshold):
                     mask[b, h, i, j] = 1
     return mask

@@ -174,3 +174,27 @@ def test_workspace_sizes_grow_with_splits():
     b = bsa.bsattn_decode_workspace_size(8, 32, 8, 128, 64, 16)
     assert b > a >= 8 * 32 * 2 * 128 * 4
     assert bsa.bsattn_prefill_workspace_size(2, 8, 4096, 4096) >= 4
+
+
+# ----------------------------------------------------------------- XAttention selection rule
+
+def test_cumulative_threshold_builder_worked_example():
+    spec = json.load(open(os.path.join(GOLDEN, "find_blocks_chunked_example.json")))
+    row = torch.tensor(spec["row"], dtype=torch.float32).view(1, 1, 1, -1)
+    got = bsa.bsattn_mask_from_cumulative_threshold(row, spec["threshold"], causal=False)
+    # the sink block is kept as well as the four picks 2, 1, 3, 4 of the example
+    assert got[0, 0, 0].tolist() == [1, 1, 1, 1, 1]
+    assert np.array_equal(got.numpy(), oracle.find_blocks_chunked(row.numpy(), spec["threshold"], False))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cumulative_threshold_builder_matches_oracle(causal):
+    g = torch.Generator().manual_seed(11)
+    x = torch.rand(2, 3, 12, 12, generator=g) ** 3          # skewed weights, like softmax sums
+    x[0, 0, 5] = 0.25                                        # ties
+    for thr in (0.3, 0.5, 0.9, 0.95, 1.0):
+        got = bsa.bsattn_mask_from_cumulative_threshold(x, thr, causal)
+        assert np.array_equal(got.numpy(), oracle.find_blocks_chunked(x.numpy(), thr, causal)), thr
+    x[1, 2, 3, 4] = float("nan")
+    with pytest.raises(bsa.BsattnError):
+        bsa.bsattn_mask_from_cumulative_threshold(x, 0.9, causal)

@@ -143,3 +143,86 @@ def test_decode_timeout_path_reports_and_recovers(bsa, c5):
     got = bsa.bsattn_decode_varlen(*args, ws=ws).cpu()
     assert bsa.bsattn_get_device_status(ws) == 0
     assert _err(got, want) <= TOL[cfg.dtype]
+
+
+# ----------------------------------------------------------------- block-mask and paged forms
+
+def _mask_of(idx, nb):
+    B, Hkv, _ = idx.shape
+    m = torch.zeros(B, Hkv, nb, dtype=torch.uint8)
+    for b in range(B):
+        for g in range(Hkv):
+            for t in idx[b, g].tolist():
+                if t >= 0:
+                    m[b, g, t] = 1
+    return m
+
+
+@pytest.mark.parametrize("ns", [0, 1, 3])
+def test_decode_mask_form(bsa, ns):
+    q, k, v, sl, idx = _small_case()
+    nb = 11
+    m = _mask_of(idx, nb)
+    m[2, 0, 9] = 1                    # past seqlen 333 (6 blocks): selects no tokens
+    dev = torch.device("cuda")
+    got = bsa.bsattn_decode_varlen_mask(q.to(dev), k.to(dev), v.to(dev), sl.to(dev), m.to(dev), ns).cpu()
+    want = oracle.decode_varlen(q, k, v, sl, oracle.decode_mask_to_indices(m))
+    assert _err(got, want) <= TOL[torch.bfloat16]
+    assert torch.equal(got, bsa.bsattn_decode_varlen_mask(q.to(dev), k.to(dev), v.to(dev), sl.to(dev),
+                                                          m.to(dev), ns).cpu())
+
+
+def test_c5_mask_form_matches_index_form(bsa, c5):
+    cfg, q, k, v, sl, idx, want = c5
+    m = _mask_of(idx, cfg.Smax // 64)
+    dev = torch.device("cuda")
+    got = bsa.bsattn_decode_varlen_mask(q.to(dev), k.to(dev), v.to(dev), sl.to(dev), m.to(dev), 16).cpu()
+    assert _err(got, want) <= TOL[cfg.dtype]
+
+
+def _paged(k, v, page, seed=1, extra=5):
+    B, Smax, Hkv, d = k.shape
+    per_seq = -(-Smax // page)
+    num_pages = B * per_seq + extra
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(num_pages, generator=g)[: B * per_seq].reshape(B, per_seq).to(torch.int32)
+    kp = torch.full((num_pages, page, Hkv, d), float("nan"), dtype=k.dtype)
+    vp = torch.full_like(kp, float("nan"))
+    for b in range(B):
+        for pg in range(per_seq):
+            seg = slice(pg * page, min((pg + 1) * page, Smax))
+            n = seg.stop - seg.start
+            kp[table[b, pg], :n] = k[b, seg]
+            vp[table[b, pg], :n] = v[b, seg]
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("page", [64, 128, 256])
+@pytest.mark.parametrize("ns", [1, 3])
+def test_decode_paged(bsa, page, ns):
+    q, k, v, sl, idx = _small_case()
+    kp, vp, table = _paged(k, v, page)
+    dev = torch.device("cuda")
+    got = bsa.bsattn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), sl.to(dev), idx.to(dev),
+                                  table.to(dev), ns).cpu()
+    want = oracle.decode_paged(q, kp, vp, sl, idx, table)
+    assert _err(got, want) <= TOL[torch.bfloat16]
+    contiguous = _run(bsa, q, k, v, sl, idx, ns)
+    assert torch.equal(got, contiguous)        # same tiles, same order: same bits
+
+
+def test_decode_paged_unmapped_page_is_flagged(bsa):
+    q, k, v, sl, idx = _small_case()
+    kp, vp, table = _paged(k, v, 128)
+    table[2, 1] = -1                           # seq 2 blocks 2-3 lose their page
+    dev = torch.device("cuda")
+    ws = bsa.workspace(dev, "decode", bsa.bsattn_decode_workspace_size(3, 8, 2, 128, 6, 2))
+    bsa.bsattn_get_device_status(ws)
+    got = bsa.bsattn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), sl.to(dev), idx.to(dev),
+                                  table.to(dev), 2).cpu()
+    assert bsa.bsattn_get_device_status(ws) & bsa.BSATTN_ERR_BAD_INDEX
+    # the oracle with those blocks removed
+    idx2 = idx.clone()
+    for gg in range(2):
+        idx2[2, gg] = torch.where((idx2[2, gg] == 2) | (idx2[2, gg] == 3), torch.tensor(-1, dtype=torch.int32), idx2[2, gg])
+    assert _err(got, oracle.decode_varlen(q, k, v, sl, idx2)) <= TOL[torch.bfloat16]
