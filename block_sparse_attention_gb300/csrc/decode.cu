@@ -72,7 +72,7 @@ struct DLayout {
     static constexpr uint32_t kMerge = 0;
     static constexpr uint32_t kMergeWarp = (16 + 8 * D) * 4;
     static constexpr uint32_t kBars = kQ + (D / 64) * 2048;
-    static constexpr uint32_t kMisc = kBars + 8 * 2 * kStages;
+    static constexpr uint32_t kMisc = kBars + 8 * (2 * kStages + 1);      // + `listed`
     static constexpr uint32_t kList = kMisc + 16;
     // two int lists per slot: logical block (sequence-end masking) and TMA row of its tile
     static uint32_t bytes(int max_slots) { return 1024 + kList + 2 * ((4 * max_slots + 15) & ~15); }
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                                              ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::kBars);
     uint64_t* empty = full + kStages;
+    uint64_t* listed = empty + kStages;          // the producer has compacted the slice
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] count, [1] abort, [2] last
     int* list = reinterpret_cast<int*>(sm + L::kList);
     const int slot_cap = (p.max_sel + p.num_splits - 1) / p.num_splits;
@@ -174,12 +175,18 @@ __global__ void __launch_bounds__(kThreads, 3)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(listed, 1);
         misc[1] = 0;
         misc[2] = 0;
         fence_barrier_init();
     }
-    if (warp == 0) {
-        // compact the slice: keep blocks 0 <= t < nb_valid and resolve the TMA row of each
+    __syncthreads();
+    float o[D / 8][4];                           // consumer state (rows lane/4 < 8 are heads)
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    if (warp == kConsumerWarps) {
+        // producer: compact the slice, keeping blocks 0 <= t < nb_valid with the TMA row of
+        // each, and start streaming at once (the consumers stage q meanwhile)
         const size_t sel_off = (static_cast<size_t>(b) * p.Hkv + g) * p.max_sel + slot0;
         int count = 0;
         bool bad = false;
@@ -221,26 +228,12 @@ __global__ void __launch_bounds__(kThreads, 3)
             count += __popc(ballot);
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, BSATTN_ERR_BAD_INDEX);
-        if (lane == 0) misc[0] = count;
-    } else if (warp == 1) {
-        // query rows of the group (G <= 8), zero-padded to 16, swizzled like the K tiles
-        const T* qg = reinterpret_cast<const T*>(p.q) + (static_cast<size_t>(b) * p.Hq + g * G) * D;
-        uint8_t* sq = sm + L::kQ;
-        for (int e = lane; e < 16 * D / 8; e += 32) {
-            const int row = e / (D / 8), col = (e % (D / 8)) * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (row < G) v = *reinterpret_cast<const uint4*>(qg + row * D + col);
-            *reinterpret_cast<uint4*>(sq + (col >> 6) * 2048 + sw128_offset(row, col & 63)) = v;
+        __syncwarp();
+        if (lane == 0) {
+            misc[0] = count;
+            mbar_arrive(listed);                 // release: list, rows and count are visible
         }
-    }
-    __syncthreads();
-    const int n = misc[0];
-
-    float o[D / 8][4];                           // consumer state (rows lane/4 < 8 are heads)
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer warp
+        const int n = count;
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
@@ -266,6 +259,20 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
     } else {
         // ------------------------------------------------------------ consumer warps 0-3
+        if (warp == 1) {
+            // query rows of the group (G <= 8), zero-padded to 16, swizzled like the K tiles
+            const T* qg = reinterpret_cast<const T*>(p.q) + (static_cast<size_t>(b) * p.Hq + g * G) * D;
+            uint8_t* sqp = sm + L::kQ;
+            for (int e = lane; e < 16 * D / 8; e += 32) {
+                const int row = e / (D / 8), col = (e % (D / 8)) * 8;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (row < G) v = *reinterpret_cast<const uint4*>(qg + row * D + col);
+                *reinterpret_cast<uint4*>(sqp + (col >> 6) * 2048 + sw128_offset(row, col & 63)) = v;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");   // consumers only
+        if (!warp_wait_parity(listed, 0, deadline, abort_flag, p.status)) ok = false;
+        const int n = ok ? misc[0] : 0;
         const float c = p.scale_log2;
         const int tok0 = 16 * warp;                 // this warp's 16 tokens of every tile
         const uint32_t sq = smem_u32(sm + L::kQ);
