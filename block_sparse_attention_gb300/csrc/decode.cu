@@ -70,7 +70,8 @@ struct DLayout {
     static constexpr uint32_t kQ = 2 * kStages * kTile;      // [16 x D] query rows (swizzled)
     // per-warp partials (m[8], l[8], O[8 x D]) reuse the K/V stages once they are drained
     static constexpr uint32_t kMerge = 0;
-    static constexpr uint32_t kMergeWarp = (16 + 8 * D) * 4;
+    static constexpr int kMergeRow = D + 8;                  // padded: 2-way bank spread
+    static constexpr uint32_t kMergeWarp = (16 + 8 * kMergeRow) * 4;
     static constexpr uint32_t kBars = kQ + (D / 64) * 2048;
     static constexpr uint32_t kMisc = kBars + 8 * (2 * kStages + 1);      // + `listed`
     static constexpr uint32_t kList = kMisc + 16;
@@ -129,6 +130,15 @@ __device__ __forceinline__ float to_f32(uint16_t raw) {
     } else {
         return __half2float(__ushort_as_half(raw));
     }
+}
+
+// Four consecutive outputs rounded to the 16-bit type in one 8-byte store.
+template <bool BF16>
+__device__ __forceinline__ void store4(void* dst, const float4 v) {
+    uint2 w;
+    w.x = pack2<BF16>(v.x, v.y);
+    w.y = pack2<BF16>(v.z, v.w);
+    *reinterpret_cast<uint2*>(dst) = w;
 }
 
 // Address (shared-space) of element (row, col) of a swizzled [rows x D] tile stored as D/64
@@ -383,72 +393,90 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) {
             const int col = nt * 8 + 2 * (lane & 3);
-            mw[16 + (lane / 4) * D + col] = o[nt][0];
-            mw[16 + (lane / 4) * D + col + 1] = o[nt][1];
+            *reinterpret_cast<float2*>(mw + 16 + (lane / 4) * L::kMergeRow + col) =
+                make_float2(o[nt][0], o[nt][1]);
         }
     }
     __syncthreads();
 
     // ---------------------------------------------------------------- combine warps, emit
-    // G rows x D columns, spread over the 128 consumer threads
+    // G rows x D columns in groups of four columns, spread over all threads
     const bool aborted = *abort_flag != 0;
     const size_t row_base = static_cast<size_t>(b) * p.Hq + g * G;   // first query head row
-    if (tid < 32 * kConsumerWarps) {
-        for (int e = tid; e < G * D; e += 32 * kConsumerWarps) {
-            const int row = e / D, col = e % D;
-            float M = -INFINITY;
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[w * (L::kMergeWarp / 4) + row]);
-            float num = 0.f, den = 0.f;
-            if (M != -INFINITY) {
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float* mw = merge + w * (L::kMergeWarp / 4);
-                    const float wt = ex2_approx(mw[row] - M);
-                    num += wt * mw[16 + row * D + col];
-                    den += wt * mw[8 + row];
-                }
+    constexpr int kW = L::kMergeWarp / 4;                             // floats per warp record
+    for (int e = tid; e < G * (D / 4); e += kThreads) {
+        const int row = e / (D / 4), c4 = e % (D / 4);
+        float mk[kConsumerWarps];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            mk[w] = merge[w * kW + row];
+            M = fmaxf(M, mk[w]);
+        }
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float wt = ex2_approx(mk[w] - M);
+                const float4 ov = *reinterpret_cast<const float4*>(merge + w * kW + 16 + row * L::kMergeRow + 4 * c4);
+                num.x += wt * ov.x;
+                num.y += wt * ov.y;
+                num.z += wt * ov.z;
+                num.w += wt * ov.w;
+                den += wt * merge[w * kW + 8 + row];
             }
-            const float val = den > 0.f ? num / den : 0.f;
-            if (p.num_splits == 1) {
-                if (!aborted)
-                    reinterpret_cast<T*>(p.out)[(row_base + row) * D + col] =
-                        BF16 ? T(__float2bfloat16_rn(val)) : T(__float2half_rn(val));
-            } else {
-                const size_t pr = (row_base + row) * p.num_splits + split;
-                p.o_part[pr * D + col] = val;
-                if (col == 0) p.lse_part[pr] = den > 0.f ? M + log2f(den) : -INFINITY;
-            }
+        }
+        const float4 val = den > 0.f ? make_float4(num.x / den, num.y / den, num.z / den, num.w / den)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.num_splits == 1) {
+            if (!aborted) store4<BF16>(reinterpret_cast<T*>(p.out) + (row_base + row) * D + 4 * c4, val);
+        } else {
+            const size_t pr = (row_base + row) * p.num_splits + split;
+            *reinterpret_cast<float4*>(p.o_part + pr * D + 4 * c4) = val;
+            if (c4 == 0) p.lse_part[pr] = den > 0.f ? M + log2f(den) : -INFINITY;
         }
     }
     if (p.num_splits == 1) return;
 
-    // last CTA of this (b, g) to arrive merges the num_splits partials
-    __threadfence();
+    // the last CTA of this (b, g) to finish merges the num_splits partials; one fence by the
+    // ticket holder after the barrier publishes every thread's partial writes
     __syncthreads();
     if (tid == 0) {
+        __threadfence();
         const int ticket = atomicAdd(&p.tickets[b * p.Hkv + g], 1);
         misc[2] = ticket == p.num_splits - 1;
+        if (misc[2]) __threadfence();
     }
     __syncthreads();
     if (!misc[2]) return;
-    __threadfence();
-    for (int e = tid; e < G * D; e += kThreads) {
-        const int row = e / D, col = e % D;
+    // partials are read through L2 only (ld.global.cg): an SM's L1 may hold stale copies from
+    // an earlier call; loads of different splits are independent, so they overlap
+    for (int e = tid; e < G * (D / 4); e += kThreads) {
+        const int row = e / (D / 4), c4 = e % (D / 4);
         const size_t r0 = (row_base + row) * p.num_splits;
-        const volatile float* lse = p.lse_part + r0;
-        const volatile float* op = p.o_part + r0 * D;
+        const float* lse = p.lse_part + r0;
+        const float4* op = reinterpret_cast<const float4*>(p.o_part + r0 * D) + c4;
         float M = -INFINITY;
-        for (int s2 = 0; s2 < p.num_splits; ++s2) M = fmaxf(M, lse[s2]);
-        float num = 0.f, den = 0.f;
+#pragma unroll 8
+        for (int s2 = 0; s2 < p.num_splits; ++s2) M = fmaxf(M, __ldcg(lse + s2));
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
         if (M != -INFINITY) {
+#pragma unroll 8
             for (int s2 = 0; s2 < p.num_splits; ++s2) {
-                const float wt = ex2_approx(lse[s2] - M);
-                num += wt * op[s2 * D + col];
+                const float wt = ex2_approx(__ldcg(lse + s2) - M);
+                const float4 ov = __ldcg(op + static_cast<size_t>(s2) * (D / 4));
+                num.x += wt * ov.x;
+                num.y += wt * ov.y;
+                num.z += wt * ov.z;
+                num.w += wt * ov.w;
                 den += wt;
             }
         }
-        const float val = den > 0.f ? num / den : 0.f;
-        reinterpret_cast<T*>(p.out)[(row_base + row) * D + col] =
-            BF16 ? T(__float2bfloat16_rn(val)) : T(__float2half_rn(val));
+        const float4 val = den > 0.f ? make_float4(num.x / den, num.y / den, num.z / den, num.w / den)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        store4<BF16>(reinterpret_cast<T*>(p.out) + (row_base + row) * D + 4 * c4, val);
     }
     if (tid == 0) p.tickets[b * p.Hkv + g] = 0;   // ready for the next call
 }
