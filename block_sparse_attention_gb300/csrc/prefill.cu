@@ -17,8 +17,8 @@
 // the longest items start first and the tail is short.  Warp roles (256 threads):
 //   warp 7      scheduler: takes the next item from the counter (once the producer has issued
 //               the previous item's loads) and compacts its mask row;
-//   warp 5      producer: loads each item's Q and streams its K and V tiles into a 3-stage K
-//               ring and a 2-stage V ring -- running ahead across item boundaries;
+//   warp 5      producer: loads each item's Q and streams its K and V tiles into two-stage K
+//               and V rings -- running ahead across item boundaries;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
 //   warp 6      issues P V as soon as the softmax has written P (two issuing threads keep the
 //               M=64 tensor pipe fed: one thread issues at most about one MMA per 50 cycles);
@@ -28,8 +28,9 @@
 //
 // Differences from the page's kernel (made for this hardware):
 //  * the mask row is compacted once per item, so masked K/V tiles are never addressed;
-//  * S is double-buffered and a K stage is released as soon as its Q K^T is done, so Q K^T
-//    of the next blocks runs while the softmax works; the next item's loads overlap the
+//  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done, so
+//    Q K^T of the next blocks runs while the softmax works, and the softmax of block g+1
+//    runs while P V of block g is in the tensor pipe; the next item's loads overlap the
 //    current item's work;
 //  * O lives in TMEM and is rescaled only when a row maximum grows by more than 2^8
 //    (exact: the final normaliser l is accumulated against the same reference maximum).
@@ -52,7 +53,7 @@ constexpr int kSWarp = 4;               // issues Q K^T, owns TMEM
 constexpr int kProdWarp = 5;            // TMA producer
 constexpr int kPVWarp = 6;              // issues P V
 constexpr int kSchedWarp = 7;           // fetches items, compacts their mask rows
-constexpr int kKStages = 3;             // K ring (a stage frees when its Q K^T is done)
+constexpr int kKStages = 2;             // K ring (a stage frees when its Q K^T is done)
 constexpr int kVStages = 2;             // V ring (a stage frees when its P V is done)
 constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
 constexpr uint32_t kOCol = 128;
@@ -97,11 +98,11 @@ struct Layout {
     static constexpr uint32_t kQ = 0;                     // Q of the current item
     static constexpr uint32_t kK = kTile;
     static constexpr uint32_t kV = kK + kKStages * kTile;
-    static constexpr uint32_t kP = kV + kVStages * kTile; // one [64 x 64] P tile
-    static constexpr uint32_t kBars = kP + 8192;
+    static constexpr uint32_t kP = kV + kVStages * kTile; // two [64 x 64] P tiles
+    static constexpr uint32_t kBars = kP + 2 * 8192;
     // q_full q_free k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] s_free[2]
-    // p_full o_done o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
-    static constexpr uint32_t kNumBars = 2 + 2 * kKStages + 2 * kVStages + 4 + 3 + 2 * kSlots + 5;
+    // p_full[2] o_done[2] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
+    static constexpr uint32_t kNumBars = 2 + 2 * kKStages + 2 * kVStages + 4 + 5 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 20 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -149,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* v_empty = v_full + kVStages;         // [VS]
     uint64_t* s_full = v_empty + kVStages;         // [2]
     uint64_t* s_free = s_full + 2;                 // [2]
-    uint64_t* p_full = s_free + 2;
-    uint64_t* o_done = p_full + 1;
-    uint64_t* o_free = o_done + 1;
+    uint64_t* p_full = s_free + 2;                 // [2] P tile g&1 written
+    uint64_t* o_done = p_full + 2;                 // [2] P V of a block g with this g&1 done
+    uint64_t* o_free = o_done + 2;
     uint64_t* item_full = o_free + 1;              // [slots]
     uint64_t* item_empty = item_full + kSlots;     // [slots]
     uint64_t* fin_s = item_empty + kSlots;
@@ -195,9 +196,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
-        mbar_init(o_free, 128);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&p_full[j], 4);                  // one arrival per softmax warp
+            mbar_init(&o_done[j], 1);
+        }
+        mbar_init(o_free, 4);
         mbar_init(fin_s, 1);
         mbar_init(fin_pv, 1);
         mbar_init(loaded, 1);
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int i = 0; i < cnt; ++i) {
                     const int g = blk + i;
                     const int vs = g % kVStages;
-                    if (!wait_parity(p_full, g & 1, deadline, abort_flag, status) ||
+                    if (!wait_parity(&p_full[g & 1], (g >> 1) & 1, deadline, abort_flag, status) ||
                         (i == 0 && items >= 1 &&
                          !wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status)) ||
                         !wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status)) {
@@ -484,11 +487,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(smem_u32(sp) + kk * 32, 16, 1024);
+                        const uint64_t a = sdesc_sw128(smem_u32(sp + (g & 1) * 8192) + kk * 32, 16, 1024);
                         const uint64_t b = sdesc_sw128(smem_u32(sv + vs * kTile) + kk * 2048, 8192, 1024);
                         mma_f16_ss(tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(o_done);          // P V of g is done: O holds it, P is free
+                    mma_commit(&o_done[g & 1]);  // P V of g is done: O holds it, P tile g&1 is free
                     mma_commit(&v_empty[vs]);
                 }
                 if (!ok) break;
@@ -503,9 +506,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
     } else {
         // ------------------------------------------------------------ softmax warps 0-3
-        const int quad = lane >> 2, qi = lane & 3;
-        const int lrowA = 16 * warp + quad;           // local rows of this thread
-        const int lrowB = lrowA + 8;
+        // Lanes t and t + 16 of warp w own local query row 16w + t%16 (TMEM lane 32w + t%16 of
+        // the M = 64 accumulator); lane t takes columns [32 (t/16), +32) of every S tile and
+        // columns [(d/2) (t/16), +d/2) of O, through the 16x32bx2 access shape.
+        const int hf = lane >> 4;
+        const int lrow = 16 * warp + (lane & 15);
         const uint32_t tl = tbase + (static_cast<uint32_t>(32 * warp) << 16);
         const float c = p.scale_log2;
         int blk = 0, qloads = 0, nsplit = 0;
@@ -530,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (lane == 0) mbar_arrive(&item_empty[slot]);
                 continue;
             }
-            const int rowA = qb * 64 + lrowA, rowB = qb * 64 + lrowB;
-            float m_used[2] = {-INFINITY, -INFINITY};
-            float l[2] = {0.f, 0.f};
+            const int row = qb * 64 + lrow;
+            float m_used = -INFINITY;
+            float l = 0.f;
             bool ok = true;
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 tc_fence_after();
                 uint32_t r[32];
-                tmem_ld_16x256b_x8(tl + sb * 64, r);
+                tmem_ld_16x32bx2_x32<32>(tl + sb * 64, r);
                 tmem_wait_ld();
                 // this warp's lanes of S[sb] are in registers: Q K^T of block g+2 may reuse it
                 tc_fence_before();
@@ -553,132 +558,107 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(r[e]);
 
-                const int key0 = static_cast<int>(list[i]) * 64;
-                if (key0 + 63 >= p.Sk || (p.causal && key0 + 63 > qb * 64 + past)) {
+                const int key0 = static_cast<int>(list[i]) * 64 + 32 * hf;
+                if (key0 + 31 >= p.Sk || (p.causal && key0 + 31 > row + past)) {
 #pragma unroll
-                    for (int rep = 0; rep < 8; ++rep)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int key = key0 + 8 * rep + 2 * qi + e;
-                            const bool inA = key < p.Sk && (!p.causal || key <= rowA + past);
-                            const bool inB = key < p.Sk && (!p.causal || key <= rowB + past);
-                            if (!inA) s[4 * rep + e] = -INFINITY;
-                            if (!inB) s[4 * rep + 2 + e] = -INFINITY;
-                        }
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = key0 + e;
+                        if (key >= p.Sk || (p.causal && key > row + past)) s[e] = -INFINITY;
+                    }
                 }
-                // row maxima as trees (rows A and B interleave in s[4 rep + 0..1 / 2..3])
-                float t8[8];
+                // row maximum: a tree over this lane's 32 columns, then the partner lane's half
+                float t16[16];
 #pragma unroll
-                for (int rep = 0; rep < 4; ++rep) {
-                    t8[rep] = fmaxf(fmaxf(s[8 * rep], s[8 * rep + 1]), fmaxf(s[8 * rep + 4], s[8 * rep + 5]));
-                    t8[4 + rep] = fmaxf(fmaxf(s[8 * rep + 2], s[8 * rep + 3]), fmaxf(s[8 * rep + 6], s[8 * rep + 7]));
-                }
-                float mx[2] = {fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
-                               fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7]))};
+                for (int e = 0; e < 16; ++e) t16[e] = fmaxf(s[e], s[e + 16]);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                }
-                float alpha[2], mc[2];
-                bool rescale_o = false;
+                for (int w2 = 8; w2 >= 1; w2 >>= 1)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const bool grow = mx[h] * c > m_used[h] * c + kRescaleLog2;
-                    const float m_new = grow ? mx[h] : m_used[h];
-                    alpha[h] = grow ? ex2_approx((m_used[h] - m_new) * c) : 1.f;
-                    if (grow && m_used[h] != -INFINITY) rescale_o = true;
-                    m_used[h] = m_new;
-                    mc[h] = m_new == -INFINITY ? 0.f : m_new * c;
-                }
+                    for (int e = 0; e < w2; ++e) t16[e] = fmaxf(t16[e], t16[e + w2]);
+                const float mx = fmaxf(t16[0], __shfl_xor_sync(0xffffffffu, t16[0], 16));
+                const bool grow = mx * c > m_used * c + kRescaleLog2;
+                const float m_new = grow ? mx : m_used;
+                const float alpha = grow ? ex2_approx((m_used - m_new) * c) : 1.f;
+                const bool rescale_o = grow && m_used != -INFINITY;
+                m_used = m_new;
+                const float mc = m_new == -INFINITY ? 0.f : m_new * c;
 #pragma unroll
-                for (int rep = 0; rep < 8; ++rep) {
-                    s[4 * rep + 0] = ex2_approx(fmaf(s[4 * rep + 0], c, -mc[0]));
-                    s[4 * rep + 1] = ex2_approx(fmaf(s[4 * rep + 1], c, -mc[0]));
-                    s[4 * rep + 2] = ex2_approx(fmaf(s[4 * rep + 2], c, -mc[1]));
-                    s[4 * rep + 3] = ex2_approx(fmaf(s[4 * rep + 3], c, -mc[1]));
-                }
+                for (int e = 0; e < 32; ++e) s[e] = ex2_approx(fmaf(s[e], c, -mc));
 #pragma unroll
-                for (int rep = 0; rep < 4; ++rep) {
-                    t8[rep] = (s[8 * rep] + s[8 * rep + 1]) + (s[8 * rep + 4] + s[8 * rep + 5]);
-                    t8[4 + rep] = (s[8 * rep + 2] + s[8 * rep + 3]) + (s[8 * rep + 6] + s[8 * rep + 7]);
-                }
-                float sum[2] = {(t8[0] + t8[1]) + (t8[2] + t8[3]), (t8[4] + t8[5]) + (t8[6] + t8[7])};
+                for (int e = 0; e < 16; ++e) t16[e] = s[e] + s[e + 16];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
-                    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
-                    l[h] = l[h] * alpha[h] + sum[h];
-                }
-                // P V of block g-1 must be done: it reads the P tile and accumulates into O
-                if (g >= 1 && !warp_wait_parity(o_done, (g - 1) & 1, deadline, abort_flag, status)) {
+                for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                    for (int e = 0; e < w2; ++e) t16[e] = t16[e] + t16[e + w2];
+                const float sum = t16[0] + __shfl_xor_sync(0xffffffffu, t16[0], 16);
+                l = l * alpha + sum;
+                uint32_t pk[16];                  // P in the input type, ready for the P tile
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(s[2 * e], s[2 * e + 1]);
+                // P tile g&1 is free once P V of block g-2 is done
+                if (g >= 2 && !warp_wait_parity(&o_done[g & 1], ((g - 2) >> 1) & 1, deadline, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 if (__any_sync(0xffffffffu, rescale_o)) {
+                    // O is scaled once it holds every block before g: P V of g-1 must be done
+                    if (g >= 1 && !warp_wait_parity(&o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, deadline,
+                                                    abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-#pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[16];
-                        tmem_ld_16x256b_x4(tl + kOCol + c0, o);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld_16x32bx2_x32<D / 2>(tl + kOCol + c0, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int rep = 0; rep < 4; ++rep) {
-                            o[4 * rep + 0] = __float_as_uint(__uint_as_float(o[4 * rep + 0]) * alpha[0]);
-                            o[4 * rep + 1] = __float_as_uint(__uint_as_float(o[4 * rep + 1]) * alpha[0]);
-                            o[4 * rep + 2] = __float_as_uint(__uint_as_float(o[4 * rep + 2]) * alpha[1]);
-                            o[4 * rep + 3] = __float_as_uint(__uint_as_float(o[4 * rep + 3]) * alpha[1]);
-                        }
-                        tmem_st_16x256b_x4(tl + kOCol + c0, o);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st_16x32bx2_x32<D / 2>(tl + kOCol + c0, o);
                     }
                     tmem_wait_st();
                 }
-                // P -> the swizzled P tile: matrix (row group, 8-column group); lane 8i + r
-                // addresses row r of matrix i of each x4 store
+                // P -> the swizzled P tile: this lane's 32 columns are 16-byte chunks 4 hf .. 4 hf + 3
+                // of its row; a chunk c of row r sits at r * 128 + (c ^ (r % 8)) * 16
+                uint8_t* prow = sp + (g & 1) * 8192 + lrow * 128;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int mi = lane >> 3, rr = lane & 7;
-                    const int row = 16 * warp + (mi & 1) * 8 + rr;
-                    const int chunk = (2 * j + (mi >> 1)) ^ rr;
-                    stsm_x4(smem_u32(sp) + row * 128 + chunk * 16,
-                            pack2<BF16>(s[8 * j + 0], s[8 * j + 1]), pack2<BF16>(s[8 * j + 2], s[8 * j + 3]),
-                            pack2<BF16>(s[8 * j + 4], s[8 * j + 5]), pack2<BF16>(s[8 * j + 6], s[8 * j + 7]));
+                for (int k = 0; k < 4; ++k) {
+                    const int chunk = (4 * hf + k) ^ (lrow & 7);
+                    *reinterpret_cast<uint4*>(prow + chunk * 16) =
+                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(p_full);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[g & 1]);
             }
             if (!ok) break;
             // ---- epilogue: O / l, written from registers straight to global memory
             const int glast = blk + cnt - 1;
-            if (!warp_wait_parity(o_done, glast & 1, deadline, abort_flag, status)) break;
+            if (!warp_wait_parity(&o_done[glast & 1], (glast >> 1) & 1, deadline, abort_flag, status)) break;
             tc_fence_after();
-            const float inv[2] = {l[0] > 0.f ? 1.f / l[0] : 0.f, l[1] > 0.f ? 1.f / l[1] : 0.f};
+            const float inv = l > 0.f ? 1.f / l : 0.f;
             if (nparts > 1) {
                 // one part of a row split across CTAs: its O / l (fp32) and log2-sum-exp go to the
                 // row's partial slots; the last part to finish merges them with LSE weights
-                float* op = p.opart + static_cast<size_t>(sbase + part) * 64 * D;
+                float* op = p.opart + static_cast<size_t>(sbase + part) * 64 * D + lrow * D + hf * (D / 2);
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[16];
-                    tmem_ld_16x256b_x4(tl + kOCol + c0, o);
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_16x32bx2_x32<D / 2>(tl + kOCol + c0, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int rep = 0; rep < 4; ++rep) {
-                        const int col = c0 + 8 * rep + 2 * qi;
-                        *reinterpret_cast<float2*>(op + lrowA * D + col) =
-                            make_float2(__uint_as_float(o[4 * rep + 0]) * inv[0], __uint_as_float(o[4 * rep + 1]) * inv[0]);
-                        *reinterpret_cast<float2*>(op + lrowB * D + col) =
-                            make_float2(__uint_as_float(o[4 * rep + 2]) * inv[1], __uint_as_float(o[4 * rep + 3]) * inv[1]);
-                    }
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(op + c0 + e) =
+                            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                        __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
                 }
                 tc_fence_before();
-                mbar_arrive(o_free);
-                if (qi == 0) {
-                    float* lp = p.lse + static_cast<size_t>(sbase + part) * 64;
-                    lp[lrowA] = l[0] > 0.f ? m_used[0] * c + log2f(l[0]) : -INFINITY;
-                    lp[lrowB] = l[1] > 0.f ? m_used[1] * c + log2f(l[1]) : -INFINITY;
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
+                if (hf == 0)
+                    p.lse[static_cast<size_t>(sbase + part) * 64 + lrow] =
+                        l > 0.f ? m_used * c + log2f(l) : -INFINITY;
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pdone);
@@ -745,48 +725,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
             } else {
-                uint32_t ob[D / 2];
-    #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[16];
-                    tmem_ld_16x256b_x4(tl + kOCol + c0, o);
+                // this lane's d/2 columns of its row, 32 at a time: packed, stored as 16-byte vectors
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
+                                                      (static_cast<size_t>(bh) * p.Sq + row) * D + hf * (D / 2));
+#pragma unroll
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_16x32bx2_x32<D / 2>(tl + kOCol + c0, o);
                     tmem_wait_ld();
-    #pragma unroll
-                    for (int rep = 0; rep < 4; ++rep) {
-                        ob[c0 / 4 + rep] = pack2<BF16>(__uint_as_float(o[4 * rep + 0]) * inv[0],
-                                                       __uint_as_float(o[4 * rep + 1]) * inv[0]);
-                        ob[c0 / 4 + 4 + rep] = pack2<BF16>(__uint_as_float(o[4 * rep + 2]) * inv[1],
-                                                           __uint_as_float(o[4 * rep + 3]) * inv[1]);
+                    if (c0 + 32 == D / 2) {
+                        // O is in registers: the next item's first P V may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(o_free);
+                    }
+                    uint32_t ob[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        ob[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    if (row < p.Sq) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[c0 / 8 + k] = make_uint4(ob[4 * k], ob[4 * k + 1], ob[4 * k + 2], ob[4 * k + 3]);
                     }
                 }
-                // O is in registers: the next item's first P V may overwrite it
-                tc_fence_before();
-                mbar_arrive(o_free);
-                // Within a quad, thread j holds column pair 2j of each 8-column group; a 4-step
-                // exchange gives thread qi the whole group qi of its rows: one 16-byte store each.
-                T* orow = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + qb * 64) * D;
-    #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32)
-    #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t* src = ob + c0 / 4 + 4 * h;
-                        uint32_t g0 = 0, g1 = 0, g2 = 0, g3 = 0;
-    #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const int want = (qi + r) & 3;          // group the reader of this lane needs
-                            const uint32_t send = want == 0 ? src[0] : want == 1 ? src[1] : want == 2 ? src[2] : src[3];
-                            const int from = (qi - r) & 3;          // its pair sits at column 8 qi + 2 from
-                            const uint32_t got = __shfl_sync(0xffffffffu, send, (lane & ~3) | from);
-                            g0 = from == 0 ? got : g0;
-                            g1 = from == 1 ? got : g1;
-                            g2 = from == 2 ? got : g2;
-                            g3 = from == 3 ? got : g3;
-                        }
-                        const int row = h == 0 ? lrowA : lrowB;
-                        if (qb * 64 + row < p.Sq)
-                            *reinterpret_cast<uint4*>(orow + static_cast<size_t>(row) * D + c0 + 8 * qi) =
-                                make_uint4(g0, g1, g2, g3);
-                    }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
