@@ -17,8 +17,8 @@
 // the longest items start first and the tail is short.  Warp roles (256 threads):
 //   warp 7      scheduler: takes the next item from the counter (once the producer has issued
 //               the previous item's loads) and compacts its mask row;
-//   warp 5      producer: loads each item's Q and streams its K and V tiles into two-stage K
-//               and V rings -- running ahead across item boundaries;
+//   warp 5      producers: lane 0 loads each item's Q and streams its K tiles, lane 1 streams
+//               its V tiles, into two-stage K and V rings -- running ahead across items;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
 //   warp 6      issues P V as soon as the softmax has written P (two issuing threads keep the
 //               M=64 tensor pipe fed: one thread issues at most about one MMA per 50 cycles);
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* item_empty = item_full + kSlots;     // [slots]
     uint64_t* fin_s = item_empty + kSlots;
     uint64_t* fin_pv = fin_s + 1;
-    uint64_t* loaded = fin_pv + 1;                 // the producer has issued an item's loads
+    uint64_t* loaded = fin_pv + 1;                 // both producer lanes issued an item's loads
     uint64_t* pdone = loaded + 1;                  // softmax warps wrote a split part's partial
     uint64_t* mdec = pdone + 1;                    // merge decision of a split row is known
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] tmem [1] abort [2..] item, count
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         for (int j = 0; j < kSlots; ++j) {
             mbar_init(&item_full[j], 1);
-            mbar_init(&item_empty[j], 3 + 4);          // producer, S and PV issuers, 4 softmax warps
+            mbar_init(&item_empty[j], 4 + 4);          // 2 producer lanes, S and PV issuers, 4 softmax warps
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(o_free, 4);
         mbar_init(fin_s, 1);
         mbar_init(fin_pv, 1);
-        mbar_init(loaded, 1);
+        mbar_init(loaded, 2);                          // K and V producer lanes
         mbar_init(pdone, 4);
         mbar_init(mdec, 1);
         misc[1] = 0;
@@ -350,11 +350,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
         }
     } else if (warp == kProdWarp) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
+        // ------------------------------------------------------------ TMA producers
+        // lane 0 streams each item's Q and K tiles, lane 1 its V tiles: the two rings drain
+        // at different points (a K stage after Q K^T, a V stage after P V), so neither stream
+        // waits for the other's slower ring
+        if (lane < 2) {
+            const bool kside = lane == 0;
+            if (kside) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+            } else {
+                tma_prefetch_desc(&tm_v);
+            }
             int kblk = 0, vblk = 0, qloads = 0;
             bool ok = true;
             for (int n = 0; ok; ++n) {
@@ -367,38 +374,42 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     int bh, qb;
                     decode_item(t, BH, p.nq, bh, qb);
                     const uint16_t* list = lists + slot * (lstride / 2);
-                    // the previous item's Q K^T must be done before its Q is overwritten
-                    if (qloads >= 1 && !wait_parity(q_free, (qloads - 1) & 1, deadline, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(q_full, kTile);
-                    for (int h = 0; h < D / 64; ++h) tma_load_3d(sq + h * 8192, &tm_q, q_full, h * 64, qb * 64, bh);
-                    ++qloads;
-                    for (int j = 0; ok && j < count; ++j) {
-                        const int kb = list[j];
-                        const int ks = kblk % kKStages;
-                        if (kblk >= kKStages &&
-                            !wait_parity(&k_empty[ks], ((kblk / kKStages) - 1) & 1, deadline, abort_flag,
-                                         status)) {
+                    if (kside) {
+                        // the previous item's Q K^T must be done before its Q is overwritten
+                        if (qloads >= 1 && !wait_parity(q_free, (qloads - 1) & 1, deadline, abort_flag, status)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&k_full[ks], kTile);
-                        for (int h = 0; h < D / 64; ++h)
-                            tma_load_3d(sk + ks * kTile + h * 8192, &tm_k, &k_full[ks], h * 64, kb * 64, bh);
-                        ++kblk;
-                        const int vs = vblk % kVStages;
-                        if (vblk >= kVStages &&
-                            !wait_parity(&v_empty[vs], ((vblk / kVStages) - 1) & 1, deadline, abort_flag,
-                                         status)) {
-                            ok = false;
-                            break;
+                        mbar_arrive_expect_tx(q_full, kTile);
+                        for (int h = 0; h < D / 64; ++h) tma_load_3d(sq + h * 8192, &tm_q, q_full, h * 64, qb * 64, bh);
+                        ++qloads;
+                        for (int j = 0; ok && j < count; ++j) {
+                            const int ks = kblk % kKStages;
+                            if (kblk >= kKStages &&
+                                !wait_parity(&k_empty[ks], ((kblk / kKStages) - 1) & 1, deadline, abort_flag,
+                                             status)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&k_full[ks], kTile);
+                            for (int h = 0; h < D / 64; ++h)
+                                tma_load_3d(sk + ks * kTile + h * 8192, &tm_k, &k_full[ks], h * 64, list[j] * 64, bh);
+                            ++kblk;
                         }
-                        mbar_arrive_expect_tx(&v_full[vs], kTile);
-                        for (int h = 0; h < D / 64; ++h)
-                            tma_load_3d(sv + vs * kTile + h * 8192, &tm_v, &v_full[vs], h * 64, kb * 64, bh);
-                        ++vblk;
+                    } else {
+                        for (int j = 0; ok && j < count; ++j) {
+                            const int vs = vblk % kVStages;
+                            if (vblk >= kVStages &&
+                                !wait_parity(&v_empty[vs], ((vblk / kVStages) - 1) & 1, deadline, abort_flag,
+                                             status)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&v_full[vs], kTile);
+                            for (int h = 0; h < D / 64; ++h)
+                                tma_load_3d(sv + vs * kTile + h * 8192, &tm_v, &v_full[vs], h * 64, list[j] * 64, bh);
+                            ++vblk;
+                        }
                     }
                 }
                 if (ok) {
@@ -409,11 +420,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (*abort_flag) {
                 // let copies already in flight land before the shared memory is released
                 const uint64_t dl = global_timer_ns() + 200000000ull;
-                if (qloads > 0) wait_parity_drain(q_full, (qloads - 1) & 1, dl);
-                for (int j = max(0, kblk - kKStages); j < kblk; ++j)
-                    wait_parity_drain(&k_full[j % kKStages], (j / kKStages) & 1, dl);
-                for (int j = max(0, vblk - kVStages); j < vblk; ++j)
-                    wait_parity_drain(&v_full[j % kVStages], (j / kVStages) & 1, dl);
+                if (kside) {
+                    if (qloads > 0) wait_parity_drain(q_full, (qloads - 1) & 1, dl);
+                    for (int j = max(0, kblk - kKStages); j < kblk; ++j)
+                        wait_parity_drain(&k_full[j % kKStages], (j / kKStages) & 1, dl);
+                } else {
+                    for (int j = max(0, vblk - kVStages); j < vblk; ++j)
+                        wait_parity_drain(&v_full[j % kVStages], (j / kVStages) & 1, dl);
+                }
             }
         }
     } else if (warp == kSWarp) {
