@@ -70,17 +70,19 @@ constexpr int kWsDone = 32;
 constexpr int kWsContHead = 48;
 constexpr int kWsPoolNext = 49;
 constexpr int kWsEpoch = 50;
+constexpr int kWsQTail = 51;
 constexpr size_t kWsHeaderBytes = 1024;
 constexpr int kMaxSlots = 2048;         // partial outputs that can be in use at once
-constexpr int kSplitMin = 96;           // rows visiting more key blocks than this are split
-constexpr int kSplitLen = 64;           // ... into parts of this many blocks
-constexpr int kSplitMinNk = 1024;       // splitting is on only when rows can be this long
+constexpr int kSplitMinNk = 1024;       // rows are split only when they can be this long
 constexpr int kEntryInts = 8;           // t, start, len, part, nparts, slot base, ready, -
 
 struct PrefillParams {
     const uint8_t* mask;
     int* ws;                            // status word + scheduler counters
     int* entries;                       // [kMaxSlots][kEntryInts]; nullptr: no splitting
+    int split_min;                      // rows visiting more key blocks than this are split
+    int split_len;                      // ... into parts of this many blocks
+    int long_row;                       // a CTA on a row longer than this claims no item ahead
     int* tickets;                       // [kMaxSlots]
     float* lse;                         // [kMaxSlots][64]
     float* opart;                       // [kMaxSlots][64][d]
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* item_empty = item_full + kSlots;     // [slots]
     uint64_t* fin_s = item_empty + kSlots;
     uint64_t* fin_pv = fin_s + 1;
-    uint64_t* loaded = fin_pv + 1;                 // both producer lanes issued an item's loads
+    uint64_t* loaded = fin_pv + 1;                 // the K lane issued an item's Q and K loads
     uint64_t* pdone = loaded + 1;                  // softmax warps wrote a split part's partial
     uint64_t* mdec = pdone + 1;                    // merge decision of a split row is known
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] tmem [1] abort [2..] item, count
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(o_free, 4);
         mbar_init(fin_s, 1);
         mbar_init(fin_pv, 1);
-        mbar_init(loaded, 2);                          // K and V producer lanes
+        mbar_init(loaded, 1);                          // the K producer lane
         mbar_init(pdone, 4);
         mbar_init(mdec, 1);
         misc[1] = 0;
@@ -222,11 +224,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // ------------------------------------------------------------ scheduler warp
         const int epoch = p.ws[kWsEpoch];
         volatile int* vws = p.ws;
+        // the next fresh item is claimed one ahead, and its mask row pulled into L2, so that
+        // neither the counter's round trip nor the row's first read delays publishing it
+        auto fresh = [&]() -> int {
+            int v = 0;
+            if (lane == 0) v = atomicAdd(p.ws + kWsNext, 1);
+            v = __shfl_sync(0xffffffffu, v, 0);
+            if (v < p.total_items) {
+                int pbh, pqb;
+                decode_item(v, BH, p.nq, pbh, pqb);
+                const uint8_t* row = p.mask + (static_cast<size_t>(pbh) * p.nq + pqb) * p.nk;
+                for (int off = lane * 128; off < p.nk; off += 32 * 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+            }
+            return v;
+        };
+        int next_t = fresh();
         for (int n = 0;; ++n) {
             const int slot = n % kSlots;
-            // take item n only once the producer has issued every load of item n-1: a CTA then
-            // holds at most one item besides the one it computes, so a CTA busy with a long
-            // item does not keep short ones from idle CTAs
+            // publish item n only once the producer has issued every K load of item n-1: a CTA
+            // then holds at most one item besides the one it computes (and one claimed ahead),
+            // so a CTA busy with a long item does not keep short ones from idle CTAs
             if (n >= 1 && !warp_wait_parity(loaded, (n - 1) & 1, deadline, abort_flag, status)) break;
             if (n >= kSlots && !warp_wait_parity(&item_empty[slot], ((n / kSlots) - 1) & 1, deadline,
                                                  abort_flag, status))
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (lane == 0 && p.entries) {
                     for (;;) {
                         const int h = vws[kWsContHead];
-                        const int tl = min(vws[kWsPoolNext], kMaxSlots);
+                        const int tl = vws[kWsQTail];
                         if (h >= tl) break;
                         if (atomicCAS(p.ws + kWsContHead, h, h + 1) != h) continue;
                         volatile int* ent = p.entries + h * kEntryInts;
@@ -254,10 +272,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         }
                         if (!ready) break;
                         __threadfence();
-                        if (ent[4] > 0) {   // a part to run (first-part entries are markers)
-                            e = h;
-                            break;
-                        }
+                        e = h;
+                        break;
                     }
                 }
                 return __shfl_sync(0xffffffffu, e, 0);
@@ -265,10 +281,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             int e = claim();
             if (*abort_flag) break;
             int t, start = 0, len = 0x7fffffff, part = 0, nparts = 1, sbase = -1;
+            bool took_fresh = false;
             if (e < 0) {
-                t = 0;
-                if (lane == 0) t = atomicAdd(p.ws + kWsNext, 1);
-                t = __shfl_sync(0xffffffffu, t, 0);
+                if (next_t < 0) next_t = fresh();   // not claimed ahead (after a long row)
+                t = next_t;
+                took_fresh = t < p.total_items;
                 if (t >= p.total_items) {
                     // no fresh rows left: parts other CTAs queued may still arrive until every
                     // CTA has taken its last row, and queued parts are always run by someone
@@ -305,38 +322,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint8_t* mrow = p.mask + (static_cast<size_t>(bh) * p.nq + qb) * p.nk;
             uint16_t* list = lists + slot * (lstride / 2);
             int count = 0;
-            for (int base = 0; base < kb_end; base += 32) {
-                const int kb = base + lane;
-                const bool on = kb < kb_end && mrow[kb] != 0;
-                const uint32_t ballot = __ballot_sync(0xffffffffu, on);
-                const int pos = count + __popc(ballot & ((1u << lane) - 1u)) - start;
-                if (on && pos >= 0 && pos < len) list[pos] = static_cast<uint16_t>(kb);
-                count += __popc(ballot);
+            for (int base = 0; base < kb_end; base += 256) {
+                // eight independent loads per lane first, then the ordered ballots
+                uint32_t bits = 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int kb = base + 32 * u + lane;
+                    if (kb < kb_end && mrow[kb] != 0) bits |= 1u << u;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int kb = base + 32 * u + lane;
+                    const bool on = (bits >> u) & 1u;
+                    const uint32_t ballot = __ballot_sync(0xffffffffu, on);
+                    const int pos = count + __popc(ballot & ((1u << lane) - 1u)) - start;
+                    if (on && pos >= 0 && pos < len) list[pos] = static_cast<uint16_t>(kb);
+                    count += __popc(ballot);
+                }
             }
             // 3. a fresh row that visits many key blocks is split: this CTA keeps the first
             //    part, the others are queued for any CTA to take
-            if (e < 0 && p.entries && count > kSplitMin) {
-                const int np = (count + kSplitLen - 1) / kSplitLen;
-                int base_slot = 0;
-                if (lane == 0) base_slot = atomicAdd(p.ws + kWsPoolNext, np);
-                base_slot = __shfl_sync(0xffffffffu, base_slot, 0);
-                const bool fits = base_slot + np <= kMaxSlots;     // else: the pool is full
-                for (int i = lane; i < np && base_slot + i < kMaxSlots; i += 32) {
-                    int* ent = p.entries + (base_slot + i) * kEntryInts;
-                    const int st = i * kSplitLen;
-                    ent[0] = t;
-                    ent[1] = st;
-                    ent[2] = min(kSplitLen, count - st);
-                    ent[3] = i;
-                    ent[4] = (i == 0 || !fits) ? 0 : np;        // markers are skipped by claimers
-                    ent[5] = base_slot;
-                    __threadfence();
-                    reinterpret_cast<volatile int*>(ent)[6] = epoch + 1;
+            if (e < 0 && p.entries && count > p.split_min) {
+                const int np = (count + p.split_len - 1) / p.split_len;
+                int base_slot = 0, q0 = 0;
+                if (lane == 0) {
+                    base_slot = atomicAdd(p.ws + kWsPoolNext, np);
+                    // queue entries only for parts 1..np-1: part 0 stays with this CTA
+                    if (base_slot + np <= kMaxSlots) q0 = atomicAdd(p.ws + kWsQTail, np - 1);
                 }
-                if (fits) {
+                base_slot = __shfl_sync(0xffffffffu, base_slot, 0);
+                q0 = __shfl_sync(0xffffffffu, q0, 0);
+                if (base_slot + np <= kMaxSlots) {               // else: the pool is full, no split
+                    for (int i = 1 + lane; i < np; i += 32) {
+                        int* ent = p.entries + (q0 + i - 1) * kEntryInts;
+                        const int st = i * p.split_len;
+                        ent[0] = t;
+                        ent[1] = st;
+                        ent[2] = min(p.split_len, count - st);
+                        ent[3] = i;
+                        ent[4] = np;
+                        ent[5] = base_slot;
+                        __threadfence();
+                        reinterpret_cast<volatile int*>(ent)[6] = epoch + 1;
+                    }
                     nparts = np;
                     sbase = base_slot;
-                    len = kSplitLen;
+                    len = p.split_len;
                 }
             }
             __syncwarp();
@@ -348,6 +379,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 sbase_of[slot] = sbase;
                 mbar_arrive(&item_full[slot]);   // release: the list is visible to the waiters
             }
+            // a long row keeps this CTA busy: claiming ahead would hold an item back from CTAs
+            // that become free sooner
+            if (took_fresh && (e >= 0 || count <= p.long_row)) next_t = fresh();
+            else if (took_fresh) next_t = -1;
         }
     } else if (warp == kProdWarp) {
         // ------------------------------------------------------------ TMA producers
@@ -413,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
                 if (ok) {
-                    mbar_arrive(loaded);
+                    if (kside) mbar_arrive(loaded);
                     mbar_arrive(&item_empty[slot]);
                 }
             }
@@ -689,52 +724,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 ++nsplit;
                 if (*reinterpret_cast<volatile int*>(merge_flag)) {
                     __threadfence();
-                    // row-wise merge: warp w takes rows 16w..16w+15; per row the part weights
-                    // are computed once and each lane streams D/32 columns of every part
-                    T* orow = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + qb * 64) * D;
-                    const float* lsr = p.lse + static_cast<size_t>(sbase) * 64;
-                    const float* opr = p.opart + static_cast<size_t>(sbase) * 64 * D;
-                    constexpr int kCols = D / 32;                 // 2 (d=64) or 4 (d=128)
-                    for (int rr = 0; rr < 16; ++rr) {
-                        const int r = 16 * warp + rr;
-                        if (qb * 64 + r >= p.Sq) break;
-                        float lp = -INFINITY;
-                        if (lane < nparts) lp = __ldcg(lsr + lane * 64 + r);
-                        float M = lp;
+                    // lanes t and t + 16 of warp w merge local row 16w + t%16, d/2 columns each,
+                    // 32 at a time: per part one weight and eight independent 16-byte loads
+                    // from L2 (where the parts' writes landed)
+                    const float* lsr = p.lse + static_cast<size_t>(sbase) * 64 + lrow;
+                    const float* opr = p.opart + (static_cast<size_t>(sbase) * 64 + lrow) * D + hf * (D / 2);
+                    float M = -INFINITY;
+#pragma unroll 4
+                    for (int pp = 0; pp < nparts; ++pp) M = fmaxf(M, __ldcg(lsr + pp * 64));
+                    float den = 0.f;
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
+                                                          (static_cast<size_t>(bh) * p.Sq + row) * D + hf * (D / 2));
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                        float acc[32];
 #pragma unroll
-                        for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-                        const float w = (M == -INFINITY || lane >= nparts) ? 0.f : ex2_approx(lp - M);
-                        float den = w;
+                        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                        if (M != -INFINITY) {
+#pragma unroll 2
+                            for (int pp = 0; pp < nparts; ++pp) {
+                                const float w = ex2_approx(__ldcg(lsr + pp * 64) - M);
+                                if (c0 == 0) den += w;
+                                const float4* src = reinterpret_cast<const float4*>(opr + static_cast<size_t>(pp) * 64 * D + c0);
 #pragma unroll
-                        for (int x = 16; x >= 1; x >>= 1) den += __shfl_xor_sync(0xffffffffu, den, x);
-                        float acc[kCols];
-#pragma unroll
-                        for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
-                        for (int pp = 0; pp < nparts; ++pp) {
-                            const float wp = __shfl_sync(0xffffffffu, w, pp & 31);
-                            const float* src = opr + static_cast<size_t>(pp) * 64 * D + r * D + lane * kCols;
-                            if constexpr (kCols == 4) {
-                                const float4 v4 = __ldcg(reinterpret_cast<const float4*>(src));
-                                acc[0] += wp * v4.x;
-                                acc[1] += wp * v4.y;
-                                acc[2] += wp * v4.z;
-                                acc[3] += wp * v4.w;
-                            } else {
-                                const float2 v2 = __ldcg(reinterpret_cast<const float2*>(src));
-                                acc[0] += wp * v2.x;
-                                acc[1] += wp * v2.y;
+                                for (int k = 0; k < 8; ++k) {
+                                    const float4 v4 = __ldcg(src + k);
+                                    acc[4 * k + 0] += w * v4.x;
+                                    acc[4 * k + 1] += w * v4.y;
+                                    acc[4 * k + 2] += w * v4.z;
+                                    acc[4 * k + 3] += w * v4.w;
+                                }
                             }
                         }
                         const float invd = den > 0.f ? 1.f / den : 0.f;
-                        uint32_t packed[kCols / 2];
+                        if (row < p.Sq) {
 #pragma unroll
-                        for (int j = 0; j < kCols / 2; ++j)
-                            packed[j] = pack2<BF16>(acc[2 * j] * invd, acc[2 * j + 1] * invd);
-                        T* dst = orow + static_cast<size_t>(r) * D + lane * kCols;
-                        if constexpr (kCols == 4) {
-                            *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-                        } else {
-                            *reinterpret_cast<uint32_t*>(dst) = packed[0];
+                            for (int k = 0; k < 4; ++k)
+                                dst[c0 / 8 + k] = make_uint4(pack2<BF16>(acc[8 * k + 0] * invd, acc[8 * k + 1] * invd),
+                                                             pack2<BF16>(acc[8 * k + 2] * invd, acc[8 * k + 3] * invd),
+                                                             pack2<BF16>(acc[8 * k + 4] * invd, acc[8 * k + 5] * invd),
+                                                             pack2<BF16>(acc[8 * k + 6] * invd, acc[8 * k + 7] * invd));
                         }
                     }
                 }
@@ -785,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             atomicExch(p.ws + kWsNext, 0);
             atomicExch(p.ws + kWsContHead, 0);
             atomicExch(p.ws + kWsPoolNext, 0);
+            atomicExch(p.ws + kWsQTail, 0);
             atomicAdd(p.ws + kWsEpoch, 1);       // queue entries of this call are now stale
             atomicExch(p.ws + kWsDone, 0);
         }
@@ -859,10 +889,14 @@ extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const
     PrefillParams prm{};
     prm.mask = block_mask;
     prm.ws = static_cast<int*>(workspace);
+    prm.long_row = nk / 2 > 32 ? nk / 2 : 32;
     if (workspace_bytes >= kWsFullBytes && nk >= kSplitMinNk) {
         // room for the continuation queue and partial outputs, and rows long enough that one
-        // of them could outlast the rest of the launch: long rows are split
+        // of them could outlast the rest of the launch: a row visiting more than 96 key blocks
+        // is split into parts of 64, run by whichever CTAs are free and merged by log-sum-exp
         uint8_t* w = static_cast<uint8_t*>(workspace);
+        prm.split_min = 96;
+        prm.split_len = 64;
         prm.entries = reinterpret_cast<int*>(w + kWsEntriesOff);
         prm.tickets = reinterpret_cast<int*>(w + kWsTicketsOff);
         prm.lse = reinterpret_cast<float*>(w + kWsLseOff);
