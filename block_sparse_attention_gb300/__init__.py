@@ -25,7 +25,7 @@ from . import build as _build
 __all__ = [
     "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA",
     "BSATTN_ERR_TIMEOUT", "BSATTN_ERR_BAD_INDEX", "BsattnError", "library_path", "load",
-    "bsattn_prefill", "bsattn_prefill_workspace_size", "bsattn_decode_varlen",
+    "bsattn_prefill", "bsattn_prefill_bs", "bsattn_prefill_workspace_size", "bsattn_decode_varlen",
     "bsattn_decode_workspace_size", "bsattn_decode_default_splits", "bsattn_num_splits_heuristic",
     "bsattn_mask_from_topk", "bsattn_mask_from_threshold", "bsattn_get_device_status",
     "bsattn_set_wait_budget_ns", "bsattn_status_string", "bsattn_version", "workspace",
@@ -70,6 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 "bsattn_status_string": ([I], ctypes.c_char_p),
                 "bsattn_version": ([], ctypes.c_char_p),
                 "bsattn_prefill": ([P, P, P, P, I, P, I, I, I, I, I, I, P, Z, P], I),
+                "bsattn_prefill_bs": ([P, P, P, P, I, I, P, I, I, I, I, I, I, P, Z, P], I),
                 "bsattn_prefill_workspace_size": ([I, I, I, I], Z),
                 "bsattn_decode_varlen": ([P, P, P, P, P, I, P, I, I, I, I, I, I, I, P, Z, P], I),
                 "bsattn_decode_workspace_size": ([I, I, I, I, I, I], Z),
@@ -145,9 +146,9 @@ def bsattn_prefill_workspace_size(B: int, H: int, Sq: int, Sk: int) -> int:
     return int(load().bsattn_prefill_workspace_size(B, H, Sq, Sk))
 
 
-def bsattn_prefill(q, k, v, block_mask, is_causal: bool, out=None, ws=None):
+def bsattn_prefill(q, k, v, block_mask, is_causal: bool, out=None, ws=None, block_size: int = 64):
     """Block-sparse attention forward.  q [B,H,Sq,d], k/v [B,H,Sk,d] fp16|bf16 CUDA;
-    block_mask [B,H,ceil(Sq/64),ceil(Sk/64)] uint8/bool CUDA."""
+    block_mask [B,H,ceil(Sq/bs),ceil(Sk/bs)] uint8/bool CUDA, bs = block_size (64 or 128)."""
     lib = load()
     for name, t in (("q", q), ("k", k), ("v", v), ("block_mask", block_mask)):
         _cuda_contig(name, t)
@@ -157,7 +158,7 @@ def bsattn_prefill(q, k, v, block_mask, is_causal: bool, out=None, ws=None):
         block_mask = block_mask.view(torch.uint8)
     if block_mask.dtype not in (torch.uint8, torch.int8):
         raise TypeError("block_mask must be uint8, int8 or bool")
-    if tuple(block_mask.shape) != (B, H, -(-Sq // 64), -(-Sk // 64)):
+    if tuple(block_mask.shape) != (B, H, -(-Sq // block_size), -(-Sk // block_size)):
         raise ValueError(f"block_mask shape {tuple(block_mask.shape)} does not match q/k")
     if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != d:
         raise ValueError("q, k, v shapes disagree")
@@ -167,9 +168,14 @@ def bsattn_prefill(q, k, v, block_mask, is_causal: bool, out=None, ws=None):
         out = torch.empty_like(q)
     if ws is None:
         ws = workspace(q.device, "prefill", bsattn_prefill_workspace_size(B, H, Sq, Sk))
-    rc = lib.bsattn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), block_mask.data_ptr(),
-                            int(bool(is_causal)), out.data_ptr(), B, H, Sq, Sk, d, _dtype_code(q),
-                            ws.data_ptr(), ws.numel(), _stream(q.device))
+    if block_size == 64:
+        rc = lib.bsattn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), block_mask.data_ptr(),
+                                int(bool(is_causal)), out.data_ptr(), B, H, Sq, Sk, d, _dtype_code(q),
+                                ws.data_ptr(), ws.numel(), _stream(q.device))
+    else:
+        rc = lib.bsattn_prefill_bs(q.data_ptr(), k.data_ptr(), v.data_ptr(), block_mask.data_ptr(),
+                                   int(block_size), int(bool(is_causal)), out.data_ptr(), B, H, Sq,
+                                   Sk, d, _dtype_code(q), ws.data_ptr(), ws.numel(), _stream(q.device))
     _check("bsattn_prefill", rc)
     return out
 

@@ -87,7 +87,9 @@ struct PrefillParams {
     float* lse;                         // [kMaxSlots][64]
     float* opart;                       // [kMaxSlots][64][d]
     void* out;
-    int B, H, Sq, Sk, nq, nk;
+    int B, H, Sq, Sk, nq, nk;           // nq, nk: 64-row query / 64-key blocks
+    int bshift;                         // mask block = 64 << bshift tokens (64 or 128)
+    int mq, mk;                         // block_mask row count and row length per (b, h)
     int causal;
     int total_items;
     float scale_log2;                   // log2(e) / sqrt(d)
@@ -233,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (v < p.total_items) {
                 int pbh, pqb;
                 decode_item(v, BH, p.nq, pbh, pqb);
-                const uint8_t* row = p.mask + (static_cast<size_t>(pbh) * p.nq + pqb) * p.nk;
-                for (int off = lane * 128; off < p.nk; off += 32 * 128)
+                const uint8_t* row = p.mask + (static_cast<size_t>(pbh) * p.mq + (pqb >> p.bshift)) * p.mk;
+                for (int off = lane * 128; off < p.mk; off += 32 * 128)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
             }
             return v;
@@ -319,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
             // 2. compact the mask row (visited key blocks in ascending order) into the slot's
             //    list, keeping entries [start, start + len) of it
-            const uint8_t* mrow = p.mask + (static_cast<size_t>(bh) * p.nq + qb) * p.nk;
+            // a mask entry covers (64 << bshift)^2 tokens: the 64-row item reads row qb >> bshift,
+            // and key block kb (64 keys) reads entry kb >> bshift of it
+            const uint8_t* mrow = p.mask + (static_cast<size_t>(bh) * p.mq + (qb >> p.bshift)) * p.mk;
             uint16_t* list = lists + slot * (lstride / 2);
             int count = 0;
             for (int base = 0; base < kb_end; base += 256) {
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int kb = base + 32 * u + lane;
-                    if (kb < kb_end && mrow[kb] != 0) bits |= 1u << u;
+                    if (kb < kb_end && mrow[kb >> p.bshift] != 0) bits |= 1u << u;
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -863,12 +867,13 @@ constexpr size_t kWsMinBytes = 256;
 
 extern "C" size_t bsattn_prefill_workspace_size(int, int, int, int) { return bsattn::kWsFullBytes; }
 
-extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
-                              int is_causal, void* out, int B, int H, int Sq, int Sk, int d,
-                              bsattn_dtype dtype, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
+                                 const uint8_t* block_mask, int block_size, int is_causal, void* out,
+                                 int B, int H, int Sq, int Sk, int d, bsattn_dtype dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
     using namespace bsattn;
     if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return BSATTN_ERR_INVALID_ARG;
+    if (block_size != 64 && block_size != 128) return BSATTN_ERR_UNSUPPORTED;
     if (d != 64 && d != 128) return BSATTN_ERR_UNSUPPORTED;
     if (dtype != BSATTN_F16 && dtype != BSATTN_BF16) return BSATTN_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < kWsMinBytes) return BSATTN_ERR_INVALID_ARG;
@@ -909,6 +914,9 @@ extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const
     prm.Sk = Sk;
     prm.nq = nq;
     prm.nk = nk;
+    prm.bshift = block_size == 128 ? 1 : 0;
+    prm.mq = (Sq + block_size - 1) / block_size;
+    prm.mk = (Sk + block_size - 1) / block_size;
     prm.causal = is_causal ? 1 : 0;
     prm.total_items = static_cast<int>(BH * nq);
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
@@ -916,4 +924,12 @@ extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const
     const bool bf16 = dtype == BSATTN_BF16;
     if (d == 64) return bf16 ? launch<64, true>(q, k, v, prm, st) : launch<64, false>(q, k, v, prm, st);
     return bf16 ? launch<128, true>(q, k, v, prm, st) : launch<128, false>(q, k, v, prm, st);
+}
+
+extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
+                              int is_causal, void* out, int B, int H, int Sq, int Sk, int d,
+                              bsattn_dtype dtype, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    return bsattn_prefill_bs(q, k, v, block_mask, 64, is_causal, out, B, H, Sq, Sk, d, dtype,
+                             workspace, workspace_bytes, stream);
 }

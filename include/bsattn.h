@@ -23,7 +23,8 @@
  *   - Workspaces must be zero-filled once before their first use; every call leaves them
  *     ready for the next call (counters are reset by the kernels themselves).  After a
  *     call reports BSATTN_ERR_TIMEOUT the workspace must be zero-filled again.
- *   - Block size is 64 tokens; head dimension d is 64 or 128; dtype fp16 or bf16.
+ *   - Block size is 64 tokens (bsattn_prefill_bs also takes 128-token prefill masks);
+ *     head dimension d is 64 or 128; dtype fp16 or bf16.
  */
 #ifndef BSATTN_H_
 #define BSATTN_H_
@@ -79,6 +80,24 @@ const char* bsattn_version(void);
 int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
                    int is_causal, void* out, int B, int H, int Sq, int Sk, int d,
                    bsattn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * bsattn_prefill with a block mask of 64- or 128-token blocks -- [BSA] 4.1-4.7 with the
+ * block size of [XA] "BSA (Block Sparse Attention)", block size requirement (the block-sparse
+ * library that consumes XAttention's selection takes 128-token blocks only).
+ *
+ *   block_size  64 or 128 (else BSATTN_ERR_UNSUPPORTED)
+ *   block_mask  (device) [B, H, ceil(Sq/block_size), ceil(Sk/block_size)] uint8: entry
+ *               [qb][kb] != 0 makes query rows [qb*bs, qb*bs+bs) see keys [kb*bs, kb*bs+bs)
+ *               (subject to the causal rule and to Sk, as in bsattn_prefill).
+ * Every other argument, the result and the error behaviour are those of bsattn_prefill, which
+ * is this call with block_size = 64.  The kernel works on 64-token tiles either way: a
+ * 128-token entry stands for the four 64 x 64 tiles it covers.
+ */
+int bsattn_prefill_bs(const void* q, const void* k, const void* v, const uint8_t* block_mask,
+                      int block_size, int is_causal, void* out, int B, int H, int Sq, int Sk,
+                      int d, bsattn_dtype dtype, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /* Workspace bytes that enable splitting long rows (256 bytes is the minimum). */
 size_t bsattn_prefill_workspace_size(int B, int H, int Sq, int Sk);

@@ -146,6 +146,9 @@ def test_prefill_rejects_bad_arguments_without_launching():
     assert _call_prefill(lib, q=(1 << 12) + 2) == bsa.BSATTN_ERR_INVALID_ARG   # misaligned
     assert _call_prefill(lib, B=-1) == bsa.BSATTN_ERR_INVALID_ARG
     assert _call_prefill(lib, Sq=0) == bsa.BSATTN_OK                          # nothing to do
+    for bs, want in ((32, bsa.BSATTN_ERR_UNSUPPORTED), (96, bsa.BSATTN_ERR_UNSUPPORTED)):
+        assert lib.bsattn_prefill_bs(1 << 12, 1 << 12, 1 << 12, 1 << 12, bs, 1, 1 << 12, 1, 1, 64,
+                                     64, 64, 0, 1 << 12, 256, None) == want
 
 
 def _call_decode(lib, **kw):

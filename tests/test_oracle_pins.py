@@ -396,3 +396,37 @@ def test_find_blocks_chunked_keeps_sink_and_diagonal():
     m = oracle.find_blocks_chunked(x, 0.05, causal=False)
     # row 2, non-causal: sink; remaining sorted 1 (0.6), 2 (0.3): take 1, then 0.6 >= 0.03
     assert m[0, 0, 2].tolist() == [1, 1, 0]
+
+
+# ----------------------------------------------------------------- 128-token mask blocks
+
+@pytest.mark.parametrize("Sq,Sk", [(128, 128), (200, 200), (130, 300), (300, 129)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_block128_brute_force(Sq, Sk, causal):
+    """A 128-token block mask against SDPA with the token mask built by kron(mask, ones(128))."""
+    g = torch.Generator().manual_seed(Sq * 7 + Sk)
+    q = torch.randn(1, 2, Sq, 16, generator=g, dtype=torch.float64)
+    k = torch.randn(1, 2, Sk, 16, generator=g, dtype=torch.float64)
+    v = torch.randn(1, 2, Sk, 16, generator=g, dtype=torch.float64)
+    bm = (torch.rand(1, 2, math.ceil(Sq / 128), math.ceil(Sk / 128), generator=g) < 0.6).to(torch.uint8)
+    tm = _token_mask(bm, Sq, Sk, causal, block=128)
+    got = oracle.prefill(q, k, v, bm, causal, block=128)
+    empty = ~tm.any(-1).numpy()
+    assert np.all(got[empty] == 0.0)
+    if (~empty).any():
+        want = _sdpa(q, k, v, tm).numpy()
+        assert np.abs(got[~empty] - want[~empty]).max() <= 1e-12
+
+
+def test_prefill_block128_equals_its_64_expansion():
+    """Each 128-token entry is the four 64-token entries it covers: same token sets, so the
+    oracle gives bit-identical results for the two forms."""
+    g = torch.Generator().manual_seed(5)
+    Sq, Sk = 333, 450
+    q, k, v = synthetic.qkv(1, 3, Sq, Sk, 64, torch.bfloat16, seed=5)
+    bm = (torch.rand(1, 3, math.ceil(Sq / 128), math.ceil(Sk / 128), generator=g) < 0.5).to(torch.uint8)
+    m64 = bm.repeat_interleave(2, dim=2).repeat_interleave(2, dim=3)[:, :, :math.ceil(Sq / 64), :math.ceil(Sk / 64)]
+    for causal in (False, True):
+        a = oracle.prefill(q, k, v, bm, causal, block=128)
+        b = oracle.prefill(q, k, v, m64, causal, block=64)
+        assert np.array_equal(a, b)

@@ -182,3 +182,31 @@ def test_long_rows_split_across_ctas(bsa):
     for h in range(H):
         want = oracle.prefill_rows(q, k, v, mask, True, 0, h, rows)
         assert _err(split[0, h, rows], want) <= TOL[torch.bfloat16]
+
+
+BS128_CASES = [
+    # B, H, Sq, Sk, d, dtype, causal, density (of the 128-token block mask)
+    (1, 2, 128, 128, 64, torch.float16, True, 0.6),
+    (2, 2, 300, 300, 128, torch.bfloat16, True, 0.5),
+    (1, 2, 130, 400, 128, torch.bfloat16, True, 0.7),      # Sq < Sk, bottom-right causal
+    (1, 3, 700, 700, 64, torch.float16, False, 0.4),
+    (1, 1, 1000, 1000, 128, torch.bfloat16, True, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,d,dtype,causal,density", BS128_CASES)
+def test_prefill_block128(bsa, B, H, Sq, Sk, d, dtype, causal, density):
+    """128-token mask blocks: parity with the oracle at block 128, and bit-identical output to
+    the same mask expanded to 64-token blocks (the kernel visits the same tiles in the same
+    order either way)."""
+    q, k, v = synthetic.qkv(B, H, Sq, Sk, d, dtype, seed=Sq + 3 * d)
+    mask = synthetic.random_block_mask(B, H, math.ceil(Sq / 128), math.ceil(Sk / 128), density,
+                                       seed=Sk + 1)
+    dev = torch.device("cuda")
+    got = bsa.bsattn_prefill(q.to(dev), k.to(dev), v.to(dev), mask.to(dev), causal,
+                             block_size=128).cpu()
+    want = oracle.prefill(q, k, v, mask, causal, block=128)
+    assert _err(got, want) <= TOL[dtype]
+    m64 = mask.repeat_interleave(2, dim=2).repeat_interleave(2, dim=3)
+    m64 = m64[:, :, :math.ceil(Sq / 64), :math.ceil(Sk / 64)].contiguous()
+    assert torch.equal(got, _run(bsa, q, k, v, m64, causal))
