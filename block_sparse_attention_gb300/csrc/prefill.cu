@@ -54,7 +54,11 @@ constexpr int kProdWarp = 5;            // TMA producer
 constexpr int kPVWarp = 6;              // issues P V
 constexpr int kSchedWarp = 7;           // fetches items, compacts their mask rows
 constexpr int kKStages = 2;             // K ring (a stage frees when its Q K^T is done)
+// K stage g % 2 and S buffer g & 1 of block g coincide, so the commit that completes S[g & 1]
+// also frees the K stage; likewise V stage g % 2 and P tile g & 1 free together (o_done)
+static_assert(kKStages == 2, "a K stage is released through the s_full barrier of its block");
 constexpr int kVStages = 2;             // V ring (a stage frees when its P V is done)
+static_assert(kVStages == 2, "a V stage is released through the o_done barrier of its block");
 constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
 constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
@@ -104,9 +108,9 @@ struct Layout {
     static constexpr uint32_t kV = kK + kKStages * kTile;
     static constexpr uint32_t kP = kV + kVStages * kTile; // two [64 x 64] P tiles
     static constexpr uint32_t kBars = kP + 2 * 8192;
-    // q_full q_free k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] s_free[2]
+    // q_full q_free k_full[KS] v_full[VS] s_full[2] s_free[2]
     // p_full[2] o_done[2] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
-    static constexpr uint32_t kNumBars = 2 + 2 * kKStages + 2 * kVStages + 4 + 5 + 2 * kSlots + 5;
+    static constexpr uint32_t kNumBars = 2 + kKStages + kVStages + 4 + 5 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 20 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -149,10 +153,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* q_full = bars;
     uint64_t* q_free = q_full + 1;
     uint64_t* k_full = q_free + 1;                 // [KS]
-    uint64_t* k_empty = k_full + kKStages;         // [KS]
-    uint64_t* v_full = k_empty + kKStages;         // [VS]
-    uint64_t* v_empty = v_full + kVStages;         // [VS]
-    uint64_t* s_full = v_empty + kVStages;         // [2]
+    uint64_t* v_full = k_full + kKStages;          // [VS]
+    uint64_t* s_full = v_full + kVStages;          // [2] (its completion also frees K stage g % 2)
     uint64_t* s_free = s_full + 2;                 // [2]
     uint64_t* p_full = s_free + 2;                 // [2] P tile g&1 written
     uint64_t* o_done = p_full + 2;                 // [2] P V of a block g with this g&1 done
@@ -194,11 +196,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&p_full[j], 4);                  // one arrival per softmax warp
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int ks = kblk % kKStages;
                             if (kblk >= kKStages &&
-                                !wait_parity(&k_empty[ks], ((kblk / kKStages) - 1) & 1, deadline, abort_flag,
+                                !wait_parity(&s_full[ks], ((kblk / kKStages) - 1) & 1, deadline, abort_flag,
                                              status)) {
                                 ok = false;
                                 break;
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int vs = vblk % kVStages;
                             if (vblk >= kVStages &&
-                                !wait_parity(&v_empty[vs], ((vblk / kVStages) - 1) & 1, deadline, abort_flag,
+                                !wait_parity(&o_done[vs], ((vblk / kVStages) - 1) & 1, deadline, abort_flag,
                                              status)) {
                                 ok = false;
                                 break;
@@ -503,7 +503,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             mma_f16_ss(tbase + (g & 1) * 64, a_base + off, b_stage + off, idS, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(&s_full[g & 1]);
-                        mma_commit(&k_empty[ks]);
                         if (i == cnt - 1) mma_commit(q_free);   // Q no longer read
                     }
                     blk += cnt;
@@ -545,7 +544,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         mma_f16_ss(tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&o_done[g & 1]);  // P V of g is done: O holds it, P tile g&1 is free
-                    mma_commit(&v_empty[vs]);
                 }
                 if (!ok) break;
                 if (cnt > 0) {
