@@ -451,28 +451,44 @@ __global__ void __launch_bounds__(kThreads, 3)
     __syncthreads();
     if (!misc[2]) return;
     // partials are read through L2 only (ld.global.cg): an SM's L1 may hold stale copies from
-    // an earlier call; loads of different splits are independent, so they overlap
+    // an earlier call.  Up to eight splits at a time, every LSE value and partial row is loaded
+    // before any is used, so one L2 round trip serves them all; an online rescale joins chunks.
     for (int e = tid; e < G * (D / 4); e += kThreads) {
         const int row = e / (D / 4), c4 = e % (D / 4);
         const size_t r0 = (row_base + row) * p.num_splits;
         const float* lse = p.lse_part + r0;
         const float4* op = reinterpret_cast<const float4*>(p.o_part + r0 * D) + c4;
-        float M = -INFINITY;
-#pragma unroll 8
-        for (int s2 = 0; s2 < p.num_splits; ++s2) M = fmaxf(M, __ldcg(lse + s2));
+        float M = -INFINITY, den = 0.f;
         float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        float den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll 8
-            for (int s2 = 0; s2 < p.num_splits; ++s2) {
-                const float wt = ex2_approx(__ldcg(lse + s2) - M);
-                const float4 ov = __ldcg(op + static_cast<size_t>(s2) * (D / 4));
-                num.x += wt * ov.x;
-                num.y += wt * ov.y;
-                num.z += wt * ov.z;
-                num.w += wt * ov.w;
+        for (int s0 = 0; s0 < p.num_splits; s0 += 8) {
+            float lv[8];
+            float4 ov[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const bool in = s0 + k < p.num_splits;
+                lv[k] = in ? __ldcg(lse + s0 + k) : -INFINITY;
+                ov[k] = in ? __ldcg(op + static_cast<size_t>(s0 + k) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float Mc = M;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) Mc = fmaxf(Mc, lv[k]);
+            if (Mc == -INFINITY) continue;
+            const float r = ex2_approx(M - Mc);          // 0 while M is still -inf
+            num.x *= r;
+            num.y *= r;
+            num.z *= r;
+            num.w *= r;
+            den *= r;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float wt = ex2_approx(lv[k] - Mc);
+                num.x += wt * ov[k].x;
+                num.y += wt * ov[k].y;
+                num.z += wt * ov[k].z;
+                num.w += wt * ov[k].w;
                 den += wt;
             }
+            M = Mc;
         }
         const float4 val = den > 0.f ? make_float4(num.x / den, num.y / den, num.z / den, num.w / den)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
