@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
-constexpr int kStages = 2;
+constexpr int kStages = 3;              // half-block (32-token) K+V stages
 constexpr size_t kHeaderBytes = 256;                   // status word + padding
 
 // Where a CTA's key blocks come from (all give the same token set semantics):
@@ -64,20 +64,22 @@ struct DecodeParams {
 
 template <int D>
 struct DLayout {
-    static constexpr uint32_t kTile = (D / 64) * 8192;      // [64 x D] 16-bit, swizzled halves
-    static constexpr uint32_t kK = 0;
-    static constexpr uint32_t kV = kStages * kTile;
-    static constexpr uint32_t kQ = 2 * kStages * kTile;      // [16 x D] query rows (swizzled)
-    // per-warp partials (m[8], l[8], O[8 x D]) reuse the K/V stages once they are drained
+    // a stage holds 32 tokens (half a block) of K and of V: per 64-column d-half one TMA box
+    // of [32 x 64] 16-bit values, 128-byte swizzled
+    static constexpr uint32_t kBox = 32 * 128;                // one [32 x 64] box
+    static constexpr uint32_t kHalfK = (D / 64) * kBox;       // K (or V) of one stage
+    static constexpr uint32_t kStage = 2 * kHalfK;            // K then V
+    // per-warp partials (m[8], l[8], O[8 x D]) reuse the stages once they are drained
     static constexpr uint32_t kMerge = 0;
     static constexpr int kMergeRow = D + 8;                  // padded: 2-way bank spread
     static constexpr uint32_t kMergeWarp = (16 + 8 * kMergeRow) * 4;
-    static constexpr uint32_t kBars = kQ + (D / 64) * 2048;
-    static constexpr uint32_t kMisc = kBars + 8 * (2 * kStages + 1);      // + `listed`
+    static constexpr uint32_t kBars = kStages * kStage;
+    // full[stage][warp pair], empty[stage], listed
+    static constexpr uint32_t kMisc = kBars + 8 * (3 * kStages + 1);
     static constexpr uint32_t kList = kMisc + 16;
     // two int lists per slot: logical block (sequence-end masking) and TMA row of its tile
     static uint32_t bytes(int max_slots) { return 1024 + kList + 2 * ((4 * max_slots + 15) & ~15); }
-    static_assert(kConsumerWarps * kMergeWarp <= 2 * kStages * kTile, "merge scratch must fit");
+    static_assert(kConsumerWarps * kMergeWarp <= kStages * kStage, "merge scratch must fit");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -92,6 +94,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one 32-bit pair per lane (lane t: row
+// t/4, columns 2 (t%4), 2 (t%4) + 1), returned in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 template <bool BF16>
@@ -149,17 +159,20 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int half_stride, in
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeParams p) {
     using L = DLayout<D>;
     using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
-    constexpr uint32_t kTile = L::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::kBars);
-    uint64_t* empty = full + kStages;
+    // Half-block hs goes to stage hs % 3 and is read by warp pair hs % 2.  Each pair waits on a
+    // full barrier of its own per stage (used every 6th half-block, always by that pair, in
+    // order): with one barrier per stage, pair 0 could wait for half-block 6 while half-block 3
+    // (pair 1) was still landing in the same stage, and parity cannot tell those phases apart.
+    uint64_t* empty = full + 2 * kStages;
     uint64_t* listed = empty + kStages;          // the producer has compacted the slice
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] count, [1] abort, [2] last
     int* list = reinterpret_cast<int*>(sm + L::kList);
@@ -181,9 +194,9 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int nslot = bps + (split < rem ? 1 : 0);
 
     if (tid == 0) {
+        for (int s = 0; s < 2 * kStages; ++s) mbar_init(&full[s], 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], kConsumerWarps / 2);   // the two warps on this half-block
         }
         mbar_init(listed, 1);
         misc[1] = 0;
@@ -191,8 +204,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         fence_barrier_init();
     }
     __syncthreads();
-    float o[D / 8][4];                           // consumer state (rows lane/4 < 8 are heads)
-    float m = -INFINITY, l = 0.f;
+    // consumer state: O^T tile fragments (row = d, column = query head) and, for the two heads
+    // 2(lane%4) and 2(lane%4)+1 of this lane, the running maximum and sum
+    float o[D / 16][4];
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     bool ok = true;
     if (warp == kConsumerWarps) {
         // producer: compact the slice, keeping blocks 0 <= t < nb_valid with the TMA row of
@@ -248,133 +263,144 @@ __global__ void __launch_bounds__(kThreads, 3)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             int issued = 0;
-            for (int j = 0; j < n; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages &&
-                    !wait_parity(&empty[st], ((j / kStages) - 1) & 1, deadline, abort_flag, p.status))
+            for (int hs = 0; hs < 2 * n; ++hs) {
+                // half-stage hs: tokens [32 (hs % 2), +32) of listed block hs / 2
+                const int st = hs % kStages;
+                if (hs >= kStages &&
+                    !wait_parity(&empty[st], ((hs / kStages) - 1) & 1, deadline, abort_flag, p.status))
                     break;
-                const int row = rows[j];
-                mbar_arrive_expect_tx(&full[st], 2 * kTile);
+                const int row = rows[hs >> 1] + 32 * (hs & 1);
+                uint8_t* stage = sm + st * L::kStage;
+                uint64_t* fb = &full[2 * st + (hs & 1)];
+                mbar_arrive_expect_tx(fb, L::kStage);
                 for (int h = 0; h < D / 64; ++h)
-                    tma_load_3d(sm + L::kK + st * kTile + h * 8192, &tm_k, &full[st], h * 64, g, row);
+                    tma_load_3d(stage + h * L::kBox, &tm_k, fb, h * 64, g, row);
                 for (int h = 0; h < D / 64; ++h)
-                    tma_load_3d(sm + L::kV + st * kTile + h * 8192, &tm_v, &full[st], h * 64, g, row);
-                issued = j + 1;
+                    tma_load_3d(stage + L::kHalfK + h * L::kBox, &tm_v, fb, h * 64, g, row);
+                issued = hs + 1;
             }
             if (*abort_flag) {
                 const uint64_t dl = global_timer_ns() + 200000000ull;
                 for (int j = max(0, issued - kStages); j < issued; ++j)
-                    wait_parity_drain(&full[j % kStages], (j / kStages) & 1, dl);
+                    wait_parity_drain(&full[2 * (j % kStages) + (j & 1)], (j / (2 * kStages)) & 1, dl);
             }
         }
     } else {
         // ------------------------------------------------------------ consumer warps 0-3
-        if (warp == 1) {
-            // query rows of the group (G <= 8), zero-padded to 16, swizzled like the K tiles
-            const T* qg = reinterpret_cast<const T*>(p.q) + (static_cast<size_t>(b) * p.Hq + g * G) * D;
-            uint8_t* sqp = sm + L::kQ;
-            for (int e = lane; e < 16 * D / 8; e += 32) {
-                const int row = e / (D / 8), col = (e % (D / 8)) * 8;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (row < G) v = *reinterpret_cast<const uint4*>(qg + row * D + col);
-                *reinterpret_cast<uint4*>(sqp + (col >> 6) * 2048 + sw128_offset(row, col & 63)) = v;
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");   // consumers only
+        // Transposed products, so that the G <= 8 query heads are the n = 8 side of each
+        // m16n8k16 MMA and no accumulator row is padding:
+        //   S^T [16 tokens x 8 heads] = K [16 tokens x d] . Q^T [d x 8 heads]
+        //   O^T [d x 8 heads]        += V^T [d x 16 tokens] . P^T [16 tokens x 8 heads]
+        // Each warp takes 16 tokens of every tile.  P^T reaches the B-operand layout of the
+        // second product through an in-register 8x8 transpose (movmatrix).
         if (!warp_wait_parity(listed, 0, deadline, abort_flag, p.status)) ok = false;
         const int n = ok ? misc[0] : 0;
         const float c = p.scale_log2;
-        const int tok0 = 16 * warp;                 // this warp's 16 tokens of every tile
-        const uint32_t sq = smem_u32(sm + L::kQ);
-        uint32_t qa[D / 16][4];
+        // warps 0-1 take the first 32 tokens of every block, warps 2-3 the last 32; a warp's
+        // 16 tokens start at row tok0 of its half-block stage
+        const int half = warp >> 1;
+        const int tok0 = 16 * (warp & 1);
+        // Q^T fragments (B operand): lane holds Q[head lane/4][d = 16 kk + 2 (lane%4) + {0,1}]
+        // and the same 8 columns further; heads >= G are zero
+        uint32_t qb[D / 16][2];
+        {
+            const T* qg = reinterpret_cast<const T*>(p.q) + (static_cast<size_t>(b) * p.Hq + g * G) * D;
+            const int hq = lane >> 2;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int mat = lane >> 3;
-            const int row = (mat & 1) * 8 + (lane & 7);
-            const int col = kk * 16 + (mat >> 1) * 8;
-            ldsm_x4(tile_addr<D>(sq, 2048, row, col), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int col = kk * 16 + 2 * (lane & 3);
+                qb[kk][0] = hq < G ? *reinterpret_cast<const uint32_t*>(qg + hq * D + col) : 0u;
+                qb[kk][1] = hq < G ? *reinterpret_cast<const uint32_t*>(qg + hq * D + col + 8) : 0u;
+            }
         }
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         for (int j = 0; j < n; ++j) {
-            const int st = j % kStages;
-            if (!warp_wait_parity(&full[st], (j / kStages) & 1, deadline, abort_flag, p.status)) {
+            const int hs = 2 * j + half;
+            const int st = hs % kStages;
+            if (!warp_wait_parity(&full[2 * st + half], (hs / (2 * kStages)) & 1, deadline, abort_flag,
+                                  p.status)) {
                 ok = false;
                 break;
             }
-            const uint32_t kbase = smem_u32(sm + L::kK + st * kTile);
-            const uint32_t vbase = smem_u32(sm + L::kV + st * kTile);
-            const int key0 = list[j] * 64 + tok0;
+            const uint32_t kbase = smem_u32(sm + st * L::kStage);
+            const uint32_t vbase = kbase + L::kHalfK;
+            const int key0 = list[j] * 64 + 32 * half + tok0;
             if (key0 + 16 > seqlen) {
                 // tokens at or past the sequence end may hold anything: zero their V rows so
                 // that P = 0 cannot meet a NaN
                 for (int e = lane; e < 16 * (D / 8); e += 32) {
                     const int r = e / (D / 8), col = (e % (D / 8)) * 8;
                     if (key0 + r >= seqlen)
-                        *reinterpret_cast<uint4*>(sm + L::kV + st * kTile + (col >> 6) * 8192 +
+                        *reinterpret_cast<uint4*>(sm + st * L::kStage + L::kHalfK + (col >> 6) * L::kBox +
                                                   sw128_offset(tok0 + r, col & 63)) =
                             make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            // S = q K^T over this warp's 16 tokens: two n-tiles of 8 tokens
-            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            // S^T: A = this warp's 16 K rows (x4: rows 0-7 | 8-15 of d 0-7, then of d 8-15)
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int mat = lane >> 3;
-                const int tok = tok0 + (mat >> 1) * 8 + (lane & 7);
-                const int col = kk * 16 + (mat & 1) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(tile_addr<D>(kbase, 8192, tok, col), b0, b1, b2, b3);
-                mma16816<BF16>(s[0], qa[kk], b0, b1);
-                mma16816<BF16>(s[1], qa[kk], b2, b3);
-            }
-            // scale to log2 units and mask tokens at or past the sequence end
-            float x[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = key0 + nt * 8 + 2 * (lane & 3) + e;
-                    x[nt * 2 + e] = key < seqlen ? s[nt][e] * c : -INFINITY;
-                }
-            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m, mx);
-            const float mref = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = ex2_approx(m - mref);
-            float pr[4], sum = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                pr[e] = ex2_approx(x[e] - mref);
-                sum += pr[e];
-            }
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            l = l * alpha + sum;
-            m = m_new;
-            // P as the A operand (rows 8-15 are padding and stay zero)
-            uint32_t pa[4];
-            pa[0] = pack2<BF16>(pr[0], pr[1]);
-            pa[1] = 0u;
-            pa[2] = pack2<BF16>(pr[2], pr[3]);
-            pa[3] = 0u;
-#pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                o[nt][0] *= alpha;
-                o[nt][1] *= alpha;
-            }
-#pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                const int mat = lane >> 3;
                 const int tok = tok0 + (mat & 1) * 8 + (lane & 7);
-                const int col = np * 16 + (mat >> 1) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(tile_addr<D>(vbase, 8192, tok, col), b0, b1, b2, b3);
-                mma16816<BF16>(o[2 * np], pa, b0, b1);
-                mma16816<BF16>(o[2 * np + 1], pa, b2, b3);
+                const int col = kk * 16 + (mat >> 1) * 8;
+                uint32_t a[4];
+                ldsm_x4(tile_addr<D>(kbase, L::kBox, tok, col), a[0], a[1], a[2], a[3]);
+                mma16816<BF16>(sc, a, qb[kk][0], qb[kk][1]);
+            }
+            // lane holds tokens t = lane/4 (sc[0..1]) and t + 8 (sc[2..3]), heads 2 (lane%4) + {0,1}
+            const int ta = key0 + (lane >> 2), tb = ta + 8;
+            float x[4];
+            x[0] = ta < seqlen ? sc[0] * c : -INFINITY;
+            x[1] = ta < seqlen ? sc[1] * c : -INFINITY;
+            x[2] = tb < seqlen ? sc[2] * c : -INFINITY;
+            x[3] = tb < seqlen ? sc[3] * c : -INFINITY;
+            float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+            }
+            float alpha[2], mref[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float m_new = fmaxf(m[h], mx[h]);
+                mref[h] = m_new == -INFINITY ? 0.f : m_new;
+                alpha[h] = ex2_approx(m[h] - mref[h]);
+                m[h] = m_new;
+            }
+            const float p0 = ex2_approx(x[0] - mref[0]), p1 = ex2_approx(x[1] - mref[1]);
+            const float p2 = ex2_approx(x[2] - mref[0]), p3 = ex2_approx(x[3] - mref[1]);
+            float sum[2] = {p0 + p2, p1 + p3};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 4);
+                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 8);
+                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 16);
+                l[h] = l[h] * alpha[h] + sum[h];
+            }
+            // P^T as the B operand: the two 8x8 (token x head) halves, transposed in registers
+            const uint32_t pb0 = movmatrix_trans(pack2<BF16>(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(pack2<BF16>(p2, p3));
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] *= alpha[0];
+                o[mt][1] *= alpha[1];
+                o[mt][2] *= alpha[0];
+                o[mt][3] *= alpha[1];
+            }
+            // O^T += V^T P^T: A = V^T from the V tile (token rows) through transposing loads
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int mat = lane >> 3;
+                const int tok = tok0 + (mat >> 1) * 8 + (lane & 7);
+                const int col = mt * 16 + (mat & 1) * 8;
+                uint32_t a[4];
+                ldsm_x4_t(tile_addr<D>(vbase, L::kBox, tok, col), a[0], a[1], a[2], a[3]);
+                mma16816<BF16>(o[mt], a, pb0, pb1);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
@@ -384,17 +410,22 @@ __global__ void __launch_bounds__(kThreads, 3)
     // become merge scratch
     __syncthreads();
     if (warp < kConsumerWarps) {
-        // per-warp partial -> shared memory (rows lane/4 < 8 hold the query heads)
+        // per-warp partial -> shared memory: [m of 8 heads | l of 8 heads | O rows of 8 heads]
         float* mw = merge + warp * (L::kMergeWarp / 4);
-        if (lane % 4 == 0) {
-            mw[lane / 4] = ok ? m : -INFINITY;
-            mw[8 + lane / 4] = ok ? l : 0.f;
+        const int h0 = 2 * (lane & 3);
+        if (lane < 4) {
+            mw[h0] = ok ? m[0] : -INFINITY;
+            mw[h0 + 1] = ok ? m[1] : -INFINITY;
+            mw[8 + h0] = ok ? l[0] : 0.f;
+            mw[8 + h0 + 1] = ok ? l[1] : 0.f;
         }
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-            const int col = nt * 8 + 2 * (lane & 3);
-            *reinterpret_cast<float2*>(mw + 16 + (lane / 4) * L::kMergeRow + col) =
-                make_float2(o[nt][0], o[nt][1]);
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int d0 = mt * 16 + (lane >> 2);
+            mw[16 + h0 * L::kMergeRow + d0] = o[mt][0];
+            mw[16 + (h0 + 1) * L::kMergeRow + d0] = o[mt][1];
+            mw[16 + h0 * L::kMergeRow + d0 + 8] = o[mt][2];
+            mw[16 + (h0 + 1) * L::kMergeRow + d0 + 8] = o[mt][3];
         }
     }
     __syncthreads();
@@ -519,8 +550,8 @@ int launch(const void* k, const void* v, const DecodeParams& prm, cudaStream_t s
     const uint64_t nrows = prm.mode == kPaged ? static_cast<uint64_t>(prm.num_pages) * prm.page_size
                                               : static_cast<uint64_t>(prm.B) * prm.Smax;
     int rc = 0;
-    rc |= encode_3d(&tk, k, BF16, D, prm.Hkv, nrows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
-    rc |= encode_3d(&tv, v, BF16, D, prm.Hkv, nrows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 64, true);
+    rc |= encode_3d(&tk, k, BF16, D, prm.Hkv, nrows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 32, true);
+    rc |= encode_3d(&tv, v, BF16, D, prm.Hkv, nrows, D * 2ull, uint64_t(prm.Hkv) * D * 2, 64, 1, 32, true);
     if (rc) return rc;
     const int slots_per_split = (prm.max_sel + prm.num_splits - 1) / prm.num_splits;
     const uint32_t smem = DLayout<D>::bytes(slots_per_split);
@@ -566,13 +597,17 @@ extern "C" int bsattn_decode_default_splits(int B, int Hkv, int max_sel, int d, 
     const long long groups = static_cast<long long>(B) * Hkv;
     if (groups <= 0 || max_sel <= 0) return 1;
     int per_sm = (d == 64 || d == 128) ? bsattn::decode_ctas_per_sm(d, max_sel) : 0;
-    if (per_sm <= 0) per_sm = 3;
-    // as many splits as fill exactly one wave of resident CTAs: every CTA streams its
-    // slice from the start, and no second, mostly empty wave follows
+    if (per_sm <= 0) per_sm = 4;
+    // at most as many splits as fill one wave of resident CTAs (every CTA streams its slice
+    // from the start, and no second, mostly empty wave follows); then the fewest splits whose
+    // largest slice is as short: 64 slots over 9 splits leave slices of 8 and 7, over 8 all 8
     long long s = static_cast<long long>(per_sm) * num_sms / groups;
     if (s > max_sel) s = max_sel;
     if (s > 64) s = 64;
-    return s < 1 ? 1 : static_cast<int>(s);
+    if (s < 1) s = 1;
+    const long long longest = (max_sel + s - 1) / s;
+    s = (max_sel + longest - 1) / longest;
+    return static_cast<int>(s);
 }
 
 extern "C" size_t bsattn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_sel,

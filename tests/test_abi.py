@@ -119,10 +119,17 @@ def test_num_splits_heuristic_matches_oracle_random():
 
 
 def test_default_splits_shape():
-    # without a GPU the library assumes 3 resident decode CTAs per SM
+    # without a GPU the library assumes 4 resident decode CTAs per SM: at most one wave
+    # (64 groups x s <= 608), then the fewest splits with the same longest slice
     s = bsa.bsattn_decode_default_splits(8, 8, 64, 128, 152)
-    assert 1 <= s <= 64 and 64 * s <= 3 * 152 < 64 * (s + 1)
+    assert s == 8 and 64 * s <= 4 * 152
     assert bsa.bsattn_decode_default_splits(1, 1, 3, 128, 152) == 3
+    for groups, max_sel in ((64, 64), (64, 50), (16, 64), (300, 64), (7, 1000)):
+        s = bsa.bsattn_decode_default_splits(groups, 1, max_sel, 128, 152)
+        cap = max(1, min(64, max_sel, 4 * 152 // groups))
+        assert 1 <= s <= cap
+        assert -(-max_sel // s) == -(-max_sel // cap)          # longest slice as short as possible
+        assert s == 1 or -(-max_sel // (s - 1)) > -(-max_sel // s)   # and the fewest splits for it
 
 
 # ----------------------------------------------------------------- argument checks (no launch)
