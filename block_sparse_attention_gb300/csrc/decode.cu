@@ -9,11 +9,12 @@
 //
 // This path is bound by HBM bandwidth (each K/V byte is used once, by G heads), so it is
 // built around bytes in flight: a producer warp streams the K and V tiles of the slice with
-// TMA (128-byte swizzle, two stages of [64 x d] K and V) while four consumer warps each take
-// 16 tokens of every tile.  The [G x 64 x d] products are small, so they run on warp-level
-// mma.sync (G query heads padded to 16 rows) straight out of the swizzled tiles.  The merge
-// is fused: the last CTA of a (b, g) group to finish (atomic ticket) combines the partials
-// and resets the ticket, so a call is a single kernel launch.
+// TMA (128-byte swizzle) into three stages of half a block (K and V of 32 tokens), four CTAs
+// per SM.  Each stage is read by a pair of consumer warps, 16 tokens each.  The [G x 64 x d]
+// products are small, so they run on warp-level mma.sync, transposed so that the G <= 8 query
+// heads are the n = 8 side of the m16n8k16 shape, straight out of the swizzled tiles.  The
+// merge is fused: the last CTA of a (b, g) group to finish (atomic ticket) combines the
+// partials and resets the ticket, so a call is a single kernel launch.
 //
 // Differences from the page's kernel: every block that crosses cache_seqlens is masked token
 // by token (the page masks only the first slot and relies on descending order), so the
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     bool ok = true;
     if (warp == kConsumerWarps) {
         // producer: compact the slice, keeping blocks 0 <= t < nb_valid with the TMA row of
-        // each, and start streaming at once (the consumers stage q meanwhile)
+        // each, and start streaming at once (the consumers load q meanwhile)
         const size_t sel_off = (static_cast<size_t>(b) * p.Hkv + g) * p.max_sel + slot0;
         int count = 0;
         bool bad = false;
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         // m16n8k16 MMA and no accumulator row is padding:
         //   S^T [16 tokens x 8 heads] = K [16 tokens x d] . Q^T [d x 8 heads]
         //   O^T [d x 8 heads]        += V^T [d x 16 tokens] . P^T [16 tokens x 8 heads]
-        // Each warp takes 16 tokens of every tile.  P^T reaches the B-operand layout of the
+        // Each warp takes 16 tokens of every block.  P^T reaches the B-operand layout of the
         // second product through an in-register 8x8 transpose (movmatrix).
         if (!warp_wait_parity(listed, 0, deadline, abort_flag, p.status)) ok = false;
         const int n = ok ? misc[0] : 0;

@@ -15,20 +15,26 @@
 // items from an atomic counter in the workspace.  Items are ordered from the last query block
 // to the first across all heads (under a causal mask the late blocks visit the most keys), so
 // the longest items start first and the tail is short.  Warp roles (256 threads):
-//   warp 7      scheduler: takes the next item from the counter (once the producer has issued
-//               the previous item's loads) and compacts its mask row;
+//   warp 7      scheduler: claims the next item from the counter one ahead (not while the CTA
+//               is on a long row) and pulls its mask row into L2; publishes it once the producer
+//               has issued the previous item's K loads, after compacting its mask row;
 //   warp 5      producers: lane 0 loads each item's Q and streams its K tiles, lane 1 streams
 //               its V tiles, into two-stage K and V rings -- running ahead across items;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
 //   warp 6      issues P V as soon as the softmax has written P (two issuing threads keep the
 //               M=64 tensor pipe fed: one thread issues at most about one MMA per 50 cycles);
-//   warps 0-3   softmax (warp w owns TMEM lanes 32w..32w+15 = query rows 16w..16w+15 of the
-//               M=64 accumulator layout) and the epilogue, which writes O / l from registers
-//               with 16-byte stores.
+//   warps 0-3   softmax (lanes t and t+16 of warp w own query row 16w + t%16, TMEM lane
+//               32w + t%16 of the M=64 accumulator, and read its two 32-column halves through
+//               the 16x32bx2 shape) and the epilogue, which writes O / l from registers with
+//               16-byte stores.
+// Rows that can span 1024+ key blocks and visit more than 96 are split into 64-block parts: the
+// CTA that compacts such a row keeps part 0 and queues the rest for free CTAs; the last part to
+// finish merges the partial outputs by log-sum-exp.
 //
 // Differences from the page's kernel (made for this hardware):
 //  * the mask row is compacted once per item, so masked K/V tiles are never addressed;
-//  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done, so
+//  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done (the
+//    commit that completes S[g & 1] frees K stage g % 2; likewise P V frees V stage g % 2), so
 //    Q K^T of the next blocks runs while the softmax works, and the softmax of block g+1
 //    runs while P V of block g is in the tensor pipe; the next item's loads overlap the
 //    current item's work;
