@@ -477,90 +477,94 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
     } else if (warp == kSWarp) {
         // ------------------------------------------------------------ Q K^T issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_f16(64, 64, BF16, false);
-            const uint64_t a_base = sdesc_sw128(smem_u32(sq), 16, 1024);
-            const uint64_t b_base = sdesc_sw128(smem_u32(sk), 16, 1024);
-            int blk = 0, qloads = 0;
-            for (int n = 0;; ++n) {
-                const int slot = n % kSlots;
-                if (!wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
-                const int item = item_of[slot];
-                const int cnt = count_of[slot];
-                if (item < 0) break;
-                bool ok = true;
-                if (cnt > 0) {
-                    if (!wait_parity(q_full, qloads & 1, deadline, abort_flag, status)) break;
-                    for (int i = 0; i < cnt; ++i) {
-                        const int g = blk + i;
-                        const int ks = g % kKStages;
-                        if (!wait_parity(&k_full[ks], (g / kKStages) & 1, deadline, abort_flag, status) ||
-                            (g >= 2 && !wait_parity(&s_free[g & 1], ((g - 2) >> 1) & 1, deadline, abort_flag,
-                                                    status))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        // descriptor start addresses advance by (byte offset >> 4)
-                        const uint64_t b_stage = b_base + ((ks * kTile) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                            mma_f16_ss(tbase + (g & 1) * 64, a_base + off, b_stage + off, idS, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&s_full[g & 1]);
-                        if (i == cnt - 1) mma_commit(q_free);   // Q no longer read
-                    }
-                    blk += cnt;
-                    ++qloads;
-                }
-                if (!ok) break;
-                mbar_arrive(&item_empty[slot]);
-            }
-            mma_commit(fin_s);
-            wait_parity_drain(fin_s, 0, global_timer_ns() + 200000000ull);
-        }
-    } else if (warp == kPVWarp) {
-        // ------------------------------------------------------------ P V issuer
-        if (lane == 0) {
-            constexpr uint32_t idO = idesc_f16(64, D, BF16, true);
-            int blk = 0, items = 0;
-            for (int n = 0;; ++n) {
-                const int slot = n % kSlots;
-                if (!wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
-                const int item = item_of[slot];
-                const int cnt = count_of[slot];
-                if (item < 0) break;
-                bool ok = true;
+        // the whole warp runs the loop and waits (converged polls are cheap); lane 0 alone
+        // issues the MMAs, commits and arrivals, under a guard predicate
+        const bool lead = lane == 0;
+        constexpr uint32_t idS = idesc_f16(64, 64, BF16, false);
+        const uint64_t a_base = sdesc_sw128(smem_u32(sq), 16, 1024);
+        const uint64_t b_base = sdesc_sw128(smem_u32(sk), 16, 1024);
+        int blk = 0, qloads = 0;
+        for (int n = 0;; ++n) {
+            const int slot = n % kSlots;
+            if (!warp_wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
+            const int item = item_of[slot];
+            const int cnt = count_of[slot];
+            if (item < 0) break;
+            bool ok = true;
+            if (cnt > 0) {
+                if (!warp_wait_parity(q_full, qloads & 1, deadline, abort_flag, status)) break;
                 for (int i = 0; i < cnt; ++i) {
                     const int g = blk + i;
-                    const int vs = g % kVStages;
-                    if (!wait_parity(&p_full[g & 1], (g >> 1) & 1, deadline, abort_flag, status) ||
-                        (i == 0 && items >= 1 &&
-                         !wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status)) ||
-                        !wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status)) {
+                    const int ks = g % kKStages;
+                    if (!warp_wait_parity(&k_full[ks], (g / kKStages) & 1, deadline, abort_flag, status) ||
+                        (g >= 2 && !warp_wait_parity(&s_free[g & 1], ((g - 2) >> 1) & 1, deadline, abort_flag,
+                                                     status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // descriptor start addresses advance by (byte offset >> 4)
+                    const uint64_t b_stage = b_base + ((ks * kTile) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(smem_u32(sp + (g & 1) * 8192) + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(smem_u32(sv + vs * kTile) + kk * 2048, 8192, 1024);
-                        mma_f16_ss(tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                        mma_f16_ss_if(lead, tbase + (g & 1) * 64, a_base + off, b_stage + off, idS,
+                                      kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&o_done[g & 1]);  // P V of g is done: O holds it, P tile g&1 is free
+                    mma_commit_if(lead, &s_full[g & 1]);
+                    if (i == cnt - 1) mma_commit_if(lead, q_free);   // Q no longer read
                 }
-                if (!ok) break;
-                if (cnt > 0) {
-                    blk += cnt;
-                    ++items;
-                }
-                mbar_arrive(&item_empty[slot]);
+                blk += cnt;
+                ++qloads;
             }
-            mma_commit(fin_pv);
-            wait_parity_drain(fin_pv, 0, global_timer_ns() + 200000000ull);
+            if (!ok) break;
+            mbar_arrive_if(lead, &item_empty[slot]);
         }
+        mma_commit_if(lead, fin_s);
+        wait_parity_drain(fin_s, 0, global_timer_ns() + 200000000ull);
+        __syncwarp();
+    } else if (warp == kPVWarp) {
+        // ------------------------------------------------------------ P V issuer
+        // converged like the Q K^T issuer: lane 0 issues under a guard predicate
+        const bool lead = lane == 0;
+        constexpr uint32_t idO = idesc_f16(64, D, BF16, true);
+        int blk = 0, items = 0;
+        for (int n = 0;; ++n) {
+            const int slot = n % kSlots;
+            if (!warp_wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
+            const int item = item_of[slot];
+            const int cnt = count_of[slot];
+            if (item < 0) break;
+            bool ok = true;
+            for (int i = 0; i < cnt; ++i) {
+                const int g = blk + i;
+                const int vs = g % kVStages;
+                if (!warp_wait_parity(&p_full[g & 1], (g >> 1) & 1, deadline, abort_flag, status) ||
+                    (i == 0 && items >= 1 &&
+                     !warp_wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status)) ||
+                    !warp_wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = sdesc_sw128(smem_u32(sp + (g & 1) * 8192) + kk * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(smem_u32(sv + vs * kTile) + kk * 2048, 8192, 1024);
+                    mma_f16_ss_if(lead, tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_if(lead, &o_done[g & 1]);  // P V of g is done: O holds it, P tile g&1 is free
+            }
+            if (!ok) break;
+            if (cnt > 0) {
+                blk += cnt;
+                ++items;
+            }
+            mbar_arrive_if(lead, &item_empty[slot]);
+        }
+        mma_commit_if(lead, fin_pv);
+        wait_parity_drain(fin_pv, 0, global_timer_ns() + 200000000ull);
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps 0-3
         // Lanes t and t + 16 of warp w own local query row 16w + t%16 (TMEM lane 32w + t%16 of

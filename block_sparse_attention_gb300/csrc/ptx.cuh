@@ -63,9 +63,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // the latter case the timeout is recorded in *status and the abort flag is raised.
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, uint64_t deadline_ns,
                                             volatile int* abort_flag, int* status) {
-    uint32_t spins = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if ((spins++ & 63u) == 0) {   // first failed poll, then every 64th
+    for (uint32_t spins = 0;; ++spins) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spins & 63u) == 0) {   // first failed poll, then every 64th
             if (*abort_flag) return false;
             if (global_timer_ns() > deadline_ns) {
                 atomicOr(status, BSATTN_ERR_TIMEOUT);
@@ -74,7 +74,6 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, uint
             }
         }
     }
-    return true;
 }
 
 // Bounded wait that ignores the abort flag: used while draining copies / MMAs that are
@@ -88,14 +87,13 @@ __device__ __forceinline__ bool wait_parity_drain(uint64_t* bar, uint32_t parity
     return true;
 }
 
-// Lane 0 of the warp waits, the verdict is broadcast: keeps the warp converged for the
-// .sync.aligned tcgen05 instructions that follow.
+// Every lane of the warp waits (a converged poll is far cheaper than one lane waiting
+// behind a branch), then the warp agrees on the verdict.
 __device__ __forceinline__ bool warp_wait_parity(uint64_t* bar, uint32_t parity,
                                                  uint64_t deadline_ns, volatile int* abort_flag,
                                                  int* status) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_parity(bar, parity, deadline_ns, abort_flag, status);
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    const bool ok = wait_parity(bar, parity, deadline_ns, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -187,11 +185,43 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// The same, issued by one lane of a converged warp: the other lanes skip it under a guard
+// predicate instead of a branch, so the warp never diverges around the issue.
+__device__ __forceinline__ void mma_f16_ss_if(bool lead, uint32_t d_tmem, uint64_t a_desc,
+                                              uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(lead ? 1u : 0u)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// tcgen05.commit / mbarrier.arrive by one lane of a converged warp, under a guard predicate.
+__device__ __forceinline__ void mma_commit_if(bool lead, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            smem_u32(bar)), "r"(lead ? 1u : 0u)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_if(bool lead, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(smem_u32(bar)),
+        "r"(lead ? 1u : 0u)
         : "memory");
 }
 
