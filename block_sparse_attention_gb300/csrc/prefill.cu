@@ -19,7 +19,8 @@
 //               is on a long row) and pulls its mask row into L2; publishes it once the producer
 //               has issued the previous item's K loads, after compacting its mask row;
 //   warp 5      producers: lane 0 loads each item's Q and streams its K tiles, lane 1 streams
-//               its V tiles, into two-stage K and V rings -- running ahead across items;
+//               its V tiles, into K and V rings (two stages at d = 128, four at d = 64) --
+//               running ahead across items;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
 //   warp 6      issues P V as soon as the softmax has written P (two issuing threads keep the
 //               M=64 tensor pipe fed: one thread issues at most about one MMA per 50 cycles);
@@ -33,11 +34,11 @@
 //
 // Differences from the page's kernel (made for this hardware):
 //  * the mask row is compacted once per item, so masked K/V tiles are never addressed;
-//  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done (the
-//    commit that completes S[g & 1] frees K stage g % 2; likewise P V frees V stage g % 2), so
-//    Q K^T of the next blocks runs while the softmax works, and the softmax of block g+1
-//    runs while P V of block g is in the tensor pipe; the next item's loads overlap the
-//    current item's work;
+//  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done (at
+//    d = 128 the commit that completes S[g & 1] frees K stage g % 2, and P V frees V stage g % 2;
+//    at d = 64 the rings are four stages deep, with their own release barriers), so Q K^T of the
+//    next blocks runs while the softmax works, and the softmax of block g+1 runs while P V of
+//    block g is in the tensor pipe; the next item's loads overlap the current item's work;
 //  * O lives in TMEM and is rescaled only when a row maximum grows by more than 2^8
 //    (exact: the final normaliser l is accumulated against the same reference maximum).
 // Every wait is bounded: on expiry the CTA records BSATTN_ERR_TIMEOUT, drains the copies and
@@ -59,12 +60,18 @@ constexpr int kSWarp = 4;               // issues Q K^T, owns TMEM
 constexpr int kProdWarp = 5;            // TMA producer
 constexpr int kPVWarp = 6;              // issues P V
 constexpr int kSchedWarp = 7;           // fetches items, compacts their mask rows
-constexpr int kKStages = 2;             // K ring (a stage frees when its Q K^T is done)
-// K stage g % 2 and S buffer g & 1 of block g coincide, so the commit that completes S[g & 1]
-// also frees the K stage; likewise V stage g % 2 and P tile g & 1 free together (o_done)
-static_assert(kKStages == 2, "a K stage is released through the s_full barrier of its block");
-constexpr int kVStages = 2;             // V ring (a stage frees when its P V is done)
-static_assert(kVStages == 2, "a V stage is released through the o_done barrier of its block");
+// K and V rings: a K stage frees when the Q K^T reading it is done, a V stage when its P V is
+// done.  At d = 128 two stages of each are what shared memory allows beside Q and P at two CTAs
+// per SM; then K stage g % 2 and S buffer g & 1 of block g coincide, so the commit that completes
+// S[g & 1] also frees the K stage (and o_done frees V stage g % 2 with P tile g & 1).  At d = 64
+// the tiles are half the size, the rings deeper, and the stages have their own k_empty / v_empty
+// barriers.
+constexpr int kRingD64 = 4;
+template <int D>
+struct Rings {
+    static constexpr int kK = D == 64 ? kRingD64 : 2;
+    static constexpr int kV = D == 64 ? kRingD64 : 2;
+};
 constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
 constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
@@ -111,12 +118,13 @@ struct Layout {
     static constexpr uint32_t kTile = (D / 64) * 8192;   // one [64 x D] 16-bit tile
     static constexpr uint32_t kQ = 0;                     // Q of the current item
     static constexpr uint32_t kK = kTile;
-    static constexpr uint32_t kV = kK + kKStages * kTile;
-    static constexpr uint32_t kP = kV + kVStages * kTile; // two [64 x 64] P tiles
+    static constexpr uint32_t kV = kK + Rings<D>::kK * kTile;
+    static constexpr uint32_t kP = kV + Rings<D>::kV * kTile; // two [64 x 64] P tiles
     static constexpr uint32_t kBars = kP + 2 * 8192;
     // q_full q_free k_full[KS] v_full[VS] s_full[2] s_free[2]
     // p_full[2] o_done[2] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
-    static constexpr uint32_t kNumBars = 2 + kKStages + kVStages + 4 + 5 + 2 * kSlots + 5;
+    // k_empty[KS] v_empty[VS]
+    static constexpr uint32_t kNumBars = 2 + 2 * (Rings<D>::kK + Rings<D>::kV) + 4 + 5 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 20 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -148,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     using L = Layout<D>;
     using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
     constexpr uint32_t kTile = L::kTile;
+    constexpr int kKStages = Rings<D>::kK;
+    constexpr int kVStages = Rings<D>::kV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -160,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* q_free = q_full + 1;
     uint64_t* k_full = q_free + 1;                 // [KS]
     uint64_t* v_full = k_full + kKStages;          // [VS]
-    uint64_t* s_full = v_full + kVStages;          // [2] (its completion also frees K stage g % 2)
+    uint64_t* s_full = v_full + kVStages;          // [2] (at d = 128 it also frees K stage g % 2)
     uint64_t* s_free = s_full + 2;                 // [2]
     uint64_t* p_full = s_free + 2;                 // [2] P tile g&1 written
     uint64_t* o_done = p_full + 2;                 // [2] P V of a block g with this g&1 done
@@ -172,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* loaded = fin_pv + 1;                 // the K lane issued an item's Q and K loads
     uint64_t* pdone = loaded + 1;                  // softmax warps wrote a split part's partial
     uint64_t* mdec = pdone + 1;                    // merge decision of a split row is known
+    uint64_t* k_empty = mdec + 1;                  // [KS] Q K^T reading the stage is done
+    uint64_t* v_empty = k_empty + kKStages;        // [VS] P V reading the stage is done
     int* misc = reinterpret_cast<int*>(sm + L::kMisc);   // [0] tmem [1] abort [2..] item, count
     int* item_of = misc + 4;                             // [slots]
     int* count_of = item_of + kSlots;                    // [slots] blocks of this (part of a) row
@@ -202,9 +214,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&p_full[j], 4);                  // one arrival per softmax warp
@@ -431,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int ks = kblk % kKStages;
                             if (kblk >= kKStages &&
-                                !wait_parity(&s_full[ks], ((kblk / kKStages) - 1) & 1, deadline, abort_flag,
+                                !wait_parity(kKStages == 2 ? &s_full[ks] : &k_empty[ks], ((kblk / kKStages) - 1) & 1,
+                                             deadline, abort_flag,
                                              status)) {
                                 ok = false;
                                 break;
@@ -445,7 +460,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int vs = vblk % kVStages;
                             if (vblk >= kVStages &&
-                                !wait_parity(&o_done[vs], ((vblk / kVStages) - 1) & 1, deadline, abort_flag,
+                                !wait_parity(kVStages == 2 ? &o_done[vs] : &v_empty[vs], ((vblk / kVStages) - 1) & 1,
+                                             deadline, abort_flag,
                                              status)) {
                                 ok = false;
                                 break;
@@ -512,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                       kk > 0 ? 1u : 0u);
                     }
                     mma_commit_if(lead, &s_full[g & 1]);
+                    if constexpr (kKStages != 2) mma_commit_if(lead, &k_empty[ks]);   // K stage free
                     if (i == cnt - 1) mma_commit_if(lead, q_free);   // Q no longer read
                 }
                 blk += cnt;
@@ -554,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     mma_f16_ss_if(lead, tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit_if(lead, &o_done[g & 1]);  // P V of g is done: O holds it, P tile g&1 is free
+                if constexpr (kVStages != 2) mma_commit_if(lead, &v_empty[vs]);   // V stage free
             }
             if (!ok) break;
             if (cnt > 0) {
