@@ -66,17 +66,22 @@ constexpr int kSchedWarp = 7;           // fetches items, compacts their mask ro
 // S[g & 1] also frees the K stage (and o_done frees V stage g % 2 with P tile g & 1).  At d = 64
 // the tiles are half the size, the rings deeper, and the stages have their own k_empty / v_empty
 // barriers.
+// At d = 128 a deeper variant trades the second P tile for a third K stage (the K stream is on
+// the critical path there, and the softmax has slack to wait for P V of the previous block); it
+// is used whenever its shared memory fits.
 constexpr int kRingD64 = 4;
-template <int D>
+template <int D, bool DEEP>
 struct Rings {
-    static constexpr int kK = D == 64 ? kRingD64 : 2;
+    static constexpr int kK = D == 64 ? kRingD64 : (DEEP ? 3 : 2);
     static constexpr int kV = D == 64 ? kRingD64 : 2;
+    static constexpr int kPTiles = (D == 128 && DEEP) ? 1 : 2;   // P tiles (double-buffered if 2)
 };
 constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
 constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
 constexpr int kCtasPerSm = 2;
 constexpr int kSlots = 3;               // items published ahead of the consumers
+constexpr uint32_t kSmemPerCtaMax = 113u * 1024u;   // dynamic shared memory at two CTAs per SM
 
 // workspace words (int): status, work counter, finished-CTA counter, continuation queue head,
 // partial-slot counter, call epoch; then the continuation entries, the per-row merge tickets,
@@ -113,18 +118,18 @@ struct PrefillParams {
     unsigned long long budget_ns;
 };
 
-template <int D>
+template <int D, bool DEEP>
 struct Layout {
     static constexpr uint32_t kTile = (D / 64) * 8192;   // one [64 x D] 16-bit tile
     static constexpr uint32_t kQ = 0;                     // Q of the current item
     static constexpr uint32_t kK = kTile;
-    static constexpr uint32_t kV = kK + Rings<D>::kK * kTile;
-    static constexpr uint32_t kP = kV + Rings<D>::kV * kTile; // two [64 x 64] P tiles
-    static constexpr uint32_t kBars = kP + 2 * 8192;
+    static constexpr uint32_t kV = kK + Rings<D, DEEP>::kK * kTile;
+    static constexpr uint32_t kP = kV + Rings<D, DEEP>::kV * kTile; // one or two [64 x 64] P tiles
+    static constexpr uint32_t kBars = kP + Rings<D, DEEP>::kPTiles * 8192;
     // q_full q_free k_full[KS] v_full[VS] s_full[2] s_free[2]
     // p_full[2] o_done[2] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
     // k_empty[KS] v_empty[VS]
-    static constexpr uint32_t kNumBars = 2 + 2 * (Rings<D>::kK + Rings<D>::kV) + 4 + 5 + 2 * kSlots + 5;
+    static constexpr uint32_t kNumBars = 2 + 2 * (Rings<D, DEEP>::kK + Rings<D, DEEP>::kV) + 4 + 5 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 20 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -149,15 +154,16 @@ __device__ __forceinline__ void decode_item(int t, int BH, int nq, int& bh, int&
     bh = t - (t / BH) * BH;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DEEP>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = Layout<D>;
+    using L = Layout<D, DEEP>;
     using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
     constexpr uint32_t kTile = L::kTile;
-    constexpr int kKStages = Rings<D>::kK;
-    constexpr int kVStages = Rings<D>::kV;
+    constexpr int kKStages = Rings<D, DEEP>::kK;
+    constexpr int kVStages = Rings<D, DEEP>::kV;
+    constexpr bool kOneP = Rings<D, DEEP>::kPTiles == 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -566,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(smem_u32(sp + (g & 1) * 8192) + kk * 32, 16, 1024);
+                    const uint64_t a = sdesc_sw128(smem_u32(sp + (kOneP ? 0 : (g & 1) * 8192)) + kk * 32, 16, 1024);
                     const uint64_t b = sdesc_sw128(smem_u32(sv + vs * kTile) + kk * 2048, 8192, 1024);
                     mma_f16_ss_if(lead, tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -673,8 +679,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 uint32_t pk[16];                  // P in the input type, ready for the P tile
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(s[2 * e], s[2 * e + 1]);
-                // P tile g&1 is free once P V of block g-2 is done
-                if (g >= 2 && !warp_wait_parity(&o_done[g & 1], ((g - 2) >> 1) & 1, deadline, abort_flag, status)) {
+                // P tile g&1 is free once P V of block g-2 is done (with one P tile: block g-1)
+                if (kOneP ? (g >= 1 && !warp_wait_parity(&o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, deadline,
+                                                         abort_flag, status))
+                          : (g >= 2 && !warp_wait_parity(&o_done[g & 1], ((g - 2) >> 1) & 1, deadline,
+                                                         abort_flag, status))) {
                     ok = false;
                     break;
                 }
@@ -699,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 // P -> the swizzled P tile: this lane's 32 columns are 16-byte chunks 4 hf .. 4 hf + 3
                 // of its row; a chunk c of row r sits at r * 128 + (c ^ (r % 8)) * 16
-                uint8_t* prow = sp + (g & 1) * 8192 + lrow * 128;
+                uint8_t* prow = sp + (kOneP ? 0 : (g & 1) * 8192) + lrow * 128;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int chunk = (4 * hf + k) ^ (lrow & 7);
@@ -851,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DEEP>
 int launch(const void* q, const void* k, const void* v, const PrefillParams& prm,
            cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
@@ -862,10 +871,10 @@ int launch(const void* q, const void* k, const void* v, const PrefillParams& prm
     rc |= encode_3d(&tv, v, BF16, D, prm.Sk, BH, D * 2ull, uint64_t(prm.Sk) * D * 2, 64, 64, 1, true);
     if (rc) return rc;
     // at most two CTAs per SM: each holds 256 of the SM's 512 TMEM columns
-    uint32_t smem = Layout<D>::bytes(prm.nk);
+    uint32_t smem = Layout<D, DEEP>::bytes(prm.nk);
     if (smem < 78u * 1024u) smem = 78u * 1024u;
-    if (smem > 113u * 1024u) return BSATTN_ERR_UNSUPPORTED;
-    auto kern = prefill_kernel<D, BF16>;
+    if (smem > kSmemPerCtaMax) return BSATTN_ERR_UNSUPPORTED;
+    auto kern = prefill_kernel<D, BF16, DEEP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSATTN_ERR_CUDA;
     int sms = num_sms_of_current_device();
@@ -948,8 +957,10 @@ extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.budget_ns = wait_budget_ns();
     const bool bf16 = dtype == BSATTN_BF16;
-    if (d == 64) return bf16 ? launch<64, true>(q, k, v, prm, st) : launch<64, false>(q, k, v, prm, st);
-    return bf16 ? launch<128, true>(q, k, v, prm, st) : launch<128, false>(q, k, v, prm, st);
+    if (d == 64) return bf16 ? launch<64, true, false>(q, k, v, prm, st) : launch<64, false, false>(q, k, v, prm, st);
+    if (Layout<128, true>::bytes(nk) <= kSmemPerCtaMax)     // the deeper K ring fits beside the lists
+        return bf16 ? launch<128, true, true>(q, k, v, prm, st) : launch<128, false, true>(q, k, v, prm, st);
+    return bf16 ? launch<128, true, false>(q, k, v, prm, st) : launch<128, false, false>(q, k, v, prm, st);
 }
 
 extern "C" int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
