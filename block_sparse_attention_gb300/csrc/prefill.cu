@@ -74,7 +74,13 @@ template <int D, bool DEEP>
 struct Rings {
     static constexpr int kK = D == 64 ? kRingD64 : (DEEP ? 3 : 2);
     static constexpr int kV = D == 64 ? kRingD64 : 2;
-    static constexpr int kPTiles = (D == 128 && DEEP) ? 1 : 2;   // P tiles (double-buffered if 2)
+    // P tiles: two (double-buffered), one in the deeper d = 128 variant.  p_full and o_done have
+    // one barrier per P tile, at least two, so that at d = 128 o_done of block g also frees V stage
+    // g % 2.  (Three P tiles at d = 64 measured 2 % slower on C4 than two.)
+    static constexpr int kPTiles = (D == 128 && DEEP) ? 1 : 2;
+    static constexpr int kPF = kPTiles > 2 ? kPTiles : 2;
+    static constexpr int kOD = kPTiles > 2 ? kPTiles : 2;
+    static_assert(kV != 2 || kOD == 2, "two V stages are released through o_done[g % 2]");
 };
 constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
 constexpr uint32_t kOCol = 128;
@@ -127,9 +133,10 @@ struct Layout {
     static constexpr uint32_t kP = kV + Rings<D, DEEP>::kV * kTile; // one or two [64 x 64] P tiles
     static constexpr uint32_t kBars = kP + Rings<D, DEEP>::kPTiles * 8192;
     // q_full q_free k_full[KS] v_full[VS] s_full[2] s_free[2]
-    // p_full[2] o_done[2] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
+    // p_full[PF] o_done[OD] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
     // k_empty[KS] v_empty[VS]
-    static constexpr uint32_t kNumBars = 2 + 2 * (Rings<D, DEEP>::kK + Rings<D, DEEP>::kV) + 4 + 5 + 2 * kSlots + 5;
+    static constexpr uint32_t kNumBars = 2 + 2 * (Rings<D, DEEP>::kK + Rings<D, DEEP>::kV) + 4 +
+                                         Rings<D, DEEP>::kPF + Rings<D, DEEP>::kOD + 1 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 20 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -163,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     constexpr uint32_t kTile = L::kTile;
     constexpr int kKStages = Rings<D, DEEP>::kK;
     constexpr int kVStages = Rings<D, DEEP>::kV;
-    constexpr bool kOneP = Rings<D, DEEP>::kPTiles == 1;
+    constexpr int kPT = Rings<D, DEEP>::kPTiles;
+    constexpr int kPF = Rings<D, DEEP>::kPF;
+    constexpr int kOD = Rings<D, DEEP>::kOD;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -178,9 +187,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* v_full = k_full + kKStages;          // [VS]
     uint64_t* s_full = v_full + kVStages;          // [2] (at d = 128 it also frees K stage g % 2)
     uint64_t* s_free = s_full + 2;                 // [2]
-    uint64_t* p_full = s_free + 2;                 // [2] P tile g&1 written
-    uint64_t* o_done = p_full + 2;                 // [2] P V of a block g with this g&1 done
-    uint64_t* o_free = o_done + 2;
+    uint64_t* p_full = s_free + 2;                 // [PF] P tile of block g written (index g % PF)
+    uint64_t* o_done = p_full + kPF;               // [OD] P V of block g done (index g % OD)
+    uint64_t* o_free = o_done + kOD;
     uint64_t* item_full = o_free + 1;              // [slots]
     uint64_t* item_empty = item_full + kSlots;     // [slots]
     uint64_t* fin_s = item_empty + kSlots;
@@ -226,10 +235,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(&p_full[j], 4);                  // one arrival per softmax warp
-            mbar_init(&o_done[j], 1);
-        }
+        for (int j = 0; j < kPF; ++j) mbar_init(&p_full[j], 4);   // one arrival per softmax warp
+        for (int j = 0; j < kOD; ++j) mbar_init(&o_done[j], 1);
         mbar_init(o_free, 4);
         mbar_init(fin_s, 1);
         mbar_init(fin_pv, 1);
@@ -551,6 +558,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // converged like the Q K^T issuer: lane 0 issues under a guard predicate
         const bool lead = lane == 0;
         constexpr uint32_t idO = idesc_f16(64, D, BF16, true);
+        const uint64_t p_desc = sdesc_sw128(smem_u32(sp), 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(smem_u32(sv), 8192, 1024);
         int blk = 0, items = 0;
         for (int n = 0;; ++n) {
             const int slot = n % kSlots;
@@ -562,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
                 const int vs = g % kVStages;
-                if (!warp_wait_parity(&p_full[g & 1], (g >> 1) & 1, deadline, abort_flag, status) ||
+                if (!warp_wait_parity(&p_full[g % kPF], (g / kPF) & 1, deadline, abort_flag, status) ||
                     (i == 0 && items >= 1 &&
                      !warp_wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status)) ||
                     !warp_wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status)) {
@@ -570,13 +579,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     break;
                 }
                 tc_fence_after();
+                // descriptor start addresses advance by (byte offset >> 4): 16 keys of P are 32 bytes
+                // along its rows, 16 tokens of V are 16 rows of 128 bytes
+                const uint64_t a0 = p_desc + static_cast<uint32_t>(g % kPT) * (8192u >> 4);
+                const uint64_t b0 = v_desc + static_cast<uint32_t>(vs) * (kTile >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(smem_u32(sp + (kOneP ? 0 : (g & 1) * 8192)) + kk * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(smem_u32(sv + vs * kTile) + kk * 2048, 8192, 1024);
-                    mma_f16_ss_if(lead, tbase + kOCol, a, b, idO, (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit_if(lead, &o_done[g & 1]);  // P V of g is done: O holds it, P tile g&1 is free
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16_ss_if(lead, tbase + kOCol, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO,
+                                  (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_if(lead, &o_done[g % kOD]);  // P V of g is done: O holds it, its P tile is free
                 if constexpr (kVStages != 2) mma_commit_if(lead, &v_empty[vs]);   // V stage free
             }
             if (!ok) break;
@@ -679,17 +690,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 uint32_t pk[16];                  // P in the input type, ready for the P tile
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(s[2 * e], s[2 * e + 1]);
-                // P tile g&1 is free once P V of block g-2 is done (with one P tile: block g-1)
-                if (kOneP ? (g >= 1 && !warp_wait_parity(&o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, deadline,
-                                                         abort_flag, status))
-                          : (g >= 2 && !warp_wait_parity(&o_done[g & 1], ((g - 2) >> 1) & 1, deadline,
-                                                         abort_flag, status))) {
+                // P tile g % PT is free once P V of block g - PT is done
+                if (g >= kPT && !warp_wait_parity(&o_done[(g - kPT) % kOD], ((g - kPT) / kOD) & 1, deadline,
+                                                  abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 if (__any_sync(0xffffffffu, rescale_o)) {
                     // O is scaled once it holds every block before g: P V of g-1 must be done
-                    if (g >= 1 && !warp_wait_parity(&o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, deadline,
+                    if (g >= 1 && !warp_wait_parity(&o_done[(g - 1) % kOD], ((g - 1) / kOD) & 1, deadline,
                                                     abort_flag, status)) {
                         ok = false;
                         break;
@@ -708,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 // P -> the swizzled P tile: this lane's 32 columns are 16-byte chunks 4 hf .. 4 hf + 3
                 // of its row; a chunk c of row r sits at r * 128 + (c ^ (r % 8)) * 16
-                uint8_t* prow = sp + (kOneP ? 0 : (g & 1) * 8192) + lrow * 128;
+                uint8_t* prow = sp + (g % kPT) * 8192 + lrow * 128;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int chunk = (4 * hf + k) ^ (lrow & 7);
@@ -718,12 +727,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[g & 1]);
+                if (lane == 0) mbar_arrive(&p_full[g % kPF]);
             }
             if (!ok) break;
             // ---- epilogue: O / l, written from registers straight to global memory
             const int glast = blk + cnt - 1;
-            if (!warp_wait_parity(&o_done[glast & 1], (glast >> 1) & 1, deadline, abort_flag, status)) break;
+            if (!warp_wait_parity(&o_done[glast % kOD], (glast / kOD) & 1, deadline, abort_flag, status)) break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             if (nparts > 1) {
