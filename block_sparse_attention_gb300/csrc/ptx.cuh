@@ -87,11 +87,25 @@ __device__ __forceinline__ bool wait_parity_drain(uint64_t* bar, uint32_t parity
     return true;
 }
 
-// Every lane of the warp waits (a converged poll is far cheaper than one lane waiting
-// behind a branch), then the warp agrees on the verdict.
+// Non-blocking probe of a phase (test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Every lane of the warp waits (a converged poll is far cheaper than one lane waiting behind a
+// branch), then the warp agrees on the verdict.
 __device__ __forceinline__ bool warp_wait_parity(uint64_t* bar, uint32_t parity,
                                                  uint64_t deadline_ns, volatile int* abort_flag,
                                                  int* status) {
+    // fast path: one non-blocking probe by every lane; the bounded loop only if it fails
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     const bool ok = wait_parity(bar, parity, deadline_ns, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
 }
