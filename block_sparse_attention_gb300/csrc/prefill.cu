@@ -143,6 +143,13 @@ struct Layout {
     static uint32_t bytes(int nk) { return 1024 + kList + kSlots * list_stride(nk); }
 };
 
+// max(a, b, c) in one instruction (three-input max.f32)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (BF16) {
@@ -662,15 +669,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         if (key >= p.Sk || (p.causal && key > row + past)) s[e] = -INFINITY;
                     }
                 }
-                // row maximum: a tree over this lane's 32 columns, then the partner lane's half
+                // row maximum: four chains of three-input maxima over this lane's 32 columns, then
+                // the partner lane's half
+                float m4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x = max3f(s[j], s[j + 4], s[j + 8]);
+                    x = max3f(x, s[j + 12], s[j + 16]);
+                    x = max3f(x, s[j + 20], s[j + 24]);
+                    m4[j] = fmaxf(x, s[j + 28]);
+                }
+                const float m0 = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
+                const float mx = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 16));
                 float t16[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) t16[e] = fmaxf(s[e], s[e + 16]);
-#pragma unroll
-                for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                    for (int e = 0; e < w2; ++e) t16[e] = fmaxf(t16[e], t16[e + w2]);
-                const float mx = fmaxf(t16[0], __shfl_xor_sync(0xffffffffu, t16[0], 16));
                 const bool grow = mx * c > m_used * c + kRescaleLog2;
                 const float m_new = grow ? mx : m_used;
                 const float alpha = grow ? ex2_approx((m_used - m_new) * c) : 1.f;
