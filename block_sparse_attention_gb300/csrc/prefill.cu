@@ -150,6 +150,27 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 
+// Packed f32x2 arithmetic (one instruction for two fp32 lanes of a register pair).
+__device__ __forceinline__ float2 fma2f(float2 a, float2 b, float2 c) {
+    unsigned long long ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+__device__ __forceinline__ float2 add2f(float2 a, float2 b) {
+    unsigned long long ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (BF16) {
@@ -681,7 +702,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 const float m0 = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
                 const float mx = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 16));
-                float t16[16];
                 const bool grow = mx * c > m_used * c + kRescaleLog2;
                 const float m_new = grow ? mx : m_used;
                 const float alpha = grow ? ex2_approx((m_used - m_new) * c) : 1.f;
@@ -689,14 +709,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 m_used = m_new;
                 const float mc = m_new == -INFINITY ? 0.f : m_new * c;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[e] = ex2_approx(fmaf(s[e], c, -mc));
+                for (int e = 0; e < 32; e += 2) {
+                    // S c - m c for two columns in one packed f32x2 FMA, then exp2 of each
+                    const float2 x = fma2f(make_float2(s[e], s[e + 1]), make_float2(c, c), make_float2(-mc, -mc));
+                    s[e] = ex2_approx(x.x);
+                    s[e + 1] = ex2_approx(x.y);
+                }
+                // row sum: a tree of packed f32x2 adds over column pairs, then the partner lane's half
+                float2 p2[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) t16[e] = s[e] + s[e + 16];
+                for (int e = 0; e < 8; ++e)
+                    p2[e] = add2f(make_float2(s[2 * e], s[2 * e + 1]), make_float2(s[2 * e + 16], s[2 * e + 17]));
 #pragma unroll
-                for (int w2 = 8; w2 >= 1; w2 >>= 1)
+                for (int w2 = 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
-                    for (int e = 0; e < w2; ++e) t16[e] = t16[e] + t16[e + w2];
-                const float sum = t16[0] + __shfl_xor_sync(0xffffffffu, t16[0], 16);
+                    for (int e = 0; e < w2; ++e) p2[e] = add2f(p2[e], p2[e + w2]);
+                const float sum0 = p2[0].x + p2[0].y;
+                const float sum = sum0 + __shfl_xor_sync(0xffffffffu, sum0, 16);
                 l = l * alpha + sum;
                 uint32_t pk[16];                  // P in the input type, ready for the P tile
 #pragma unroll
