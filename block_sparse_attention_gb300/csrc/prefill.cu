@@ -19,15 +19,19 @@
 //               is on a long row) and pulls its mask row into L2; publishes it once the producer
 //               has issued the previous item's K loads, after compacting its mask row;
 //   warp 5      producers: lane 0 loads each item's Q and streams its K tiles, lane 1 streams
-//               its V tiles, into K and V rings (two stages at d = 128, four at d = 64) --
-//               running ahead across items;
+//               its V tiles, into K and V rings -- running ahead across items.  Two stages
+//               each at d = 128 (three K stages and one P tile in the deeper variant, used
+//               whenever its shared memory fits), four each at d = 64;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
 //   warp 6      issues P V as soon as the softmax has written P (two issuing threads keep the
-//               M=64 tensor pipe fed: one thread issues at most about one MMA per 50 cycles);
+//               M=64 tensor pipe fed: one thread issues at most about one MMA per 67 cycles);
+//               warps 4 and 6 run converged, lane 0 issuing under a guard predicate;
 //   warps 0-3   softmax (lanes t and t+16 of warp w own query row 16w + t%16, TMEM lane
 //               32w + t%16 of the M=64 accumulator, and read its two 32-column halves through
-//               the 16x32bx2 shape) and the epilogue, which writes O / l from registers with
-//               16-byte stores.
+//               the 16x32bx2 shape; three-input max, packed f32x2 FMA and adds) and the
+//               epilogue, which writes O / l from registers with 16-byte stores.
+// Every mbarrier wait is polled by the whole warp (one non-blocking probe, then a bounded loop):
+// a wait by one lane behind a branch costs several times more on this hardware.
 // Rows that can span 1024+ key blocks and visit more than 96 are split into 64-block parts: the
 // CTA that compacts such a row keeps part 0 and queues the rest for free CTAs; the last part to
 // finish merges the partial outputs by log-sum-exp.
@@ -36,7 +40,7 @@
 //  * the mask row is compacted once per item, so masked K/V tiles are never addressed;
 //  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done (at
 //    d = 128 the commit that completes S[g & 1] frees K stage g % 2, and P V frees V stage g % 2;
-//    at d = 64 the rings are four stages deep, with their own release barriers), so Q K^T of the
+//    deeper rings have their own release barriers), so Q K^T of the
 //    next blocks runs while the softmax works, and the softmax of block g+1 runs while P V of
 //    block g is in the tensor pipe; the next item's loads overlap the current item's work;
 //  * O lives in TMEM and is rescaled only when a row maximum grows by more than 2^8
