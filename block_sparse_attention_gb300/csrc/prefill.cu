@@ -70,14 +70,15 @@ constexpr int kSchedWarp = 7;           // fetches items, compacts their mask ro
 // S[g & 1] also frees the K stage (and o_done frees V stage g % 2 with P tile g & 1).  At d = 64
 // the tiles are half the size, the rings deeper, and the stages have their own k_empty / v_empty
 // barriers.
-// At d = 128 a deeper variant trades the second P tile for a third K stage (the K stream is on
-// the critical path there, and the softmax has slack to wait for P V of the previous block); it
-// is used whenever its shared memory fits.
+// The deeper variants are used whenever their shared memory (which grows with the mask-row lists)
+// fits: at d = 128 a third K stage in place of the second P tile (the K stream is on the critical
+// path there, and the softmax has slack to wait for P V of the previous block); at d = 64 four
+// K and four V stages.
 constexpr int kRingD64 = 4;
 template <int D, bool DEEP>
 struct Rings {
-    static constexpr int kK = D == 64 ? kRingD64 : (DEEP ? 3 : 2);
-    static constexpr int kV = D == 64 ? kRingD64 : 2;
+    static constexpr int kK = D == 64 ? (DEEP ? kRingD64 : 2) : (DEEP ? 3 : 2);
+    static constexpr int kV = D == 64 ? (DEEP ? kRingD64 : 2) : 2;
     // P tiles: two (double-buffered), one in the deeper d = 128 variant.  p_full and o_done have
     // one barrier per P tile, at least two, so that at d = 128 o_done of block g also frees V stage
     // g % 2.  (Three P tiles at d = 64 measured 2 % slower on C4 than two.)
@@ -1010,8 +1011,14 @@ extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.budget_ns = wait_budget_ns();
     const bool bf16 = dtype == BSATTN_BF16;
-    if (d == 64) return bf16 ? launch<64, true, false>(q, k, v, prm, st) : launch<64, false, false>(q, k, v, prm, st);
-    if (Layout<128, true>::bytes(nk) <= kSmemPerCtaMax)     // the deeper K ring fits beside the lists
+    // the deeper rings whenever they fit beside the mask-row lists (up to 4024 key blocks at
+    // d = 64, 1304 at d = 128), else two stages (up to 2672 key blocks at d = 128)
+    if (d == 64) {
+        if (Layout<64, true>::bytes(nk) <= kSmemPerCtaMax)
+            return bf16 ? launch<64, true, true>(q, k, v, prm, st) : launch<64, false, true>(q, k, v, prm, st);
+        return bf16 ? launch<64, true, false>(q, k, v, prm, st) : launch<64, false, false>(q, k, v, prm, st);
+    }
+    if (Layout<128, true>::bytes(nk) <= kSmemPerCtaMax)
         return bf16 ? launch<128, true, true>(q, k, v, prm, st) : launch<128, false, true>(q, k, v, prm, st);
     return bf16 ? launch<128, true, false>(q, k, v, prm, st) : launch<128, false, false>(q, k, v, prm, st);
 }

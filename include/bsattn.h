@@ -75,7 +75,9 @@ const char* bsattn_version(void);
  *               split into 64-block parts run by different CTAs and merged by log-sum-exp
  *               (2048 partial slots; rows that do not fit run whole, so results are
  *               bit-reproducible only while the slots suffice).
- * q, k, v, out must be 16-byte aligned.  Returns BSATTN_OK or an error status.
+ * q, k, v, out must be 16-byte aligned.  Returns BSATTN_OK or an error status; Sk beyond
+ * 4096 key blocks at d = 64, or 2672 key blocks (171008 keys) at d = 128, returns
+ * BSATTN_ERR_UNSUPPORTED (the per-CTA shared memory holds each item's mask-row list).
  */
 int bsattn_prefill(const void* q, const void* k, const void* v, const uint8_t* block_mask,
                    int is_causal, void* out, int B, int H, int Sq, int Sk, int d,

@@ -184,6 +184,22 @@ def test_long_rows_split_across_ctas(bsa):
         assert _err(split[0, h, rows], want) <= TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("S,d", [(96000, 128), (258000, 64)])
+def test_wide_masks_run_the_two_stage_kernels(bsa, S, d):
+    """Masks too wide for the deeper rings' shared memory (more than 1304 key blocks at d = 128,
+    more than 4024 at d = 64) run the kernels with two-stage K/V rings: sampled rows match the
+    oracle."""
+    dev = torch.device("cuda")
+    dtype = torch.bfloat16 if d == 128 else torch.float16
+    q, k, v = synthetic.qkv(1, 1, S, S, d, dtype, seed=23)
+    nb = math.ceil(S / 64)
+    mask = synthetic.random_block_mask(1, 1, nb, nb, 0.02, seed=23)
+    got = bsa.bsattn_prefill(*[t.to(dev) for t in (q, k, v, mask)], True).cpu()
+    rows = [0, 777, S // 2 + 5, S - 1]
+    want = oracle.prefill_rows(q, k, v, mask, True, 0, 0, rows)
+    assert _err(got[0, 0, rows], want) <= TOL[dtype]
+
+
 BS128_CASES = [
     # B, H, Sq, Sk, d, dtype, causal, density (of the 128-token block mask)
     (1, 2, 128, 128, 64, torch.float16, True, 0.6),
