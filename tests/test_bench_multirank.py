@@ -59,3 +59,25 @@ def test_reference_arm_runs_on_rank_zero_only():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """bench.py reports ncu DRAM traffic only while the hash of the kernel's sources (the .cu file
+    and the inline PTX helpers it includes) matches the one recorded with the counters."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "block_sparse_attention_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_bytes(b"kernel source\n")
+    (csrc / "h.cuh").write_bytes(b"helpers\n")
+    digest = hashlib.sha256(b"kernel source\nhelpers\n").hexdigest()[:16]
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"k": {"source": ["k.cu", "h.cuh"], "source_sha256_16": digest, "bytes_per_launch": 1234}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("k") == 1234
+    assert bench.traffic_record("missing") is None
+    (csrc / "h.cuh").write_bytes(b"helpers, changed\n")
+    assert bench.traffic_record("k") is None
