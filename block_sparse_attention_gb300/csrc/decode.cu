@@ -786,6 +786,11 @@ extern "C" int bsattn_decode_varlen_noalloc(const void* q, const void* k, const 
     if (ns > max_sel && max_sel > 0) ns = max_sel;
     const size_t need = bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, ns);
     if (need > kNoAllocScratchBytes) return BSATTN_ERR_UNSUPPORTED;   // shape beyond the array
+    // the array's address is per device: the stream must run on the device it was looked up on
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return BSATTN_ERR_CUDA;
+    if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return BSATTN_ERR_CUDA;
+    if (sdev != cur) return BSATTN_ERR_INVALID_ARG;
     void* scratch = nullptr;
     int rc = noalloc_scratch(&scratch);
     if (rc) return rc;

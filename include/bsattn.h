@@ -122,7 +122,7 @@ size_t bsattn_prefill_workspace_size(int B, int H, int Sq, int Sk);
  *                  past the sequence end are skipped and flagged BSATTN_ERR_BAD_INDEX.
  *   num_splits     >= 1, or 0 to let the library choose (bsattn_decode_default_splits)
  *   out            (device) [B, Hq, d] dtype
- *   workspace      (device) >= bsattn_decode_workspace_size(B, Hq, Hkv, d, num_splits)
+ *   workspace      (device) >= bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, num_splits)
  *                  bytes, zero-filled once.
  * Requires Hq % Hkv == 0, 1 <= Hq / Hkv <= 8, d in {64, 128}; q, k, v, out 16-byte aligned.
  */
@@ -144,11 +144,15 @@ int bsattn_decode_varlen(const void* q, const void* k, const void* v,
  * (bsattn_decode_workspace_size) exceeds it return BSATTN_ERR_UNSUPPORTED.  It allocates
  * nothing: no cudaMalloc / cudaFree, no allocating library routine.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Each call clears the array's
- * status word and merge tickets with cudaMemsetAsync on `stream`.  All calls share the
- * array, so calls that overlap on the GPU (different streams, or threads) race and must be
- * serialised by the caller.  Device-detected conditions (a skipped out-of-range index, an
- * expired wait) are not reported by this variant.
+ * current; make that first call before any stream capture.  CUDA loads a library's device
+ * code lazily by default, and that first call is also what loads this file's code and
+ * reserves the array on the device: make one call per device before entering a context
+ * that must not allocate (or run with CUDA_MODULE_LOADING=EAGER).  `stream` must belong to
+ * the current device (else BSATTN_ERR_INVALID_ARG).  Each call clears the array's status
+ * word and merge tickets with cudaMemsetAsync on `stream`.  All calls share the array, so
+ * calls that overlap on the GPU (different streams, or threads) race and must be serialised
+ * by the caller.  Device-detected conditions (a skipped out-of-range index, an expired
+ * wait) are not reported by this variant.
  */
 int bsattn_decode_varlen_noalloc(const void* q, const void* k, const void* v,
                                  const int32_t* cache_seqlens, const int32_t* block_indices,

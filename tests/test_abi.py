@@ -179,6 +179,22 @@ def test_decode_rejects_bad_arguments_without_launching():
     assert _call_decode(lib, B=0) == bsa.BSATTN_OK
 
 
+def test_noalloc_decode_rejects_shapes_beyond_its_scratch_without_launching():
+    """The allocation-free decode keeps its split partials in a fixed 8 MiB array: a shape
+    whose decode workspace exceeds it is refused before any device work."""
+    lib = bsa.load()
+    f = lib.bsattn_decode_varlen_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, P]
+    f.restype = I
+    B, Hq, Hkv, d, max_sel, ns = 64, 64, 8, 128, 64, 64
+    assert bsa.bsattn_decode_workspace_size(B, Hq, Hkv, d, max_sel, ns) > (8 << 20)
+    x = 1 << 12
+    assert f(x, x, x, x, x, ns, x, B, Hq, Hkv, 65536, d, max_sel, 1, None) == \
+        bsa.BSATTN_ERR_UNSUPPORTED
+    assert f(x, x, x, x, x, -1, x, 1, 4, 1, 64, d, 1, 1, None) == bsa.BSATTN_ERR_INVALID_ARG
+
+
 def test_workspace_sizes_grow_with_splits():
     a = bsa.bsattn_decode_workspace_size(8, 32, 8, 128, 64, 2)
     b = bsa.bsattn_decode_workspace_size(8, 32, 8, 128, 64, 16)

@@ -63,7 +63,8 @@ def test_reference_arm_runs_on_rank_zero_only():
 
 def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     """bench.py reports ncu DRAM traffic only while the hash of the kernel's sources (the .cu file
-    and the inline PTX helpers it includes) matches the one recorded with the counters."""
+    and the inline PTX helpers it includes) matches the one recorded with the counters, and only
+    for the workload the counters were taken on."""
     import hashlib
     sys.path.insert(0, ROOT)
     import bench
@@ -74,10 +75,12 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     digest = hashlib.sha256(b"kernel source\nhelpers\n").hexdigest()[:16]
     prof = tmp_path / "profiles"
     prof.mkdir()
-    rec = {"k": {"source": ["k.cu", "h.cuh"], "source_sha256_16": digest, "bytes_per_launch": 1234}}
+    rec = {"k": {"source": ["k.cu", "h.cuh"], "source_sha256_16": digest, "bytes_per_launch": 1234,
+                 "config": "C3"}}
     (prof / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_record("k") == 1234
-    assert bench.traffic_record("missing") is None
+    assert bench.traffic_record("k", "C3") == 1234
+    assert bench.traffic_record("k", "C2") is None          # taken on another workload
+    assert bench.traffic_record("missing", "C3") is None
     (csrc / "h.cuh").write_bytes(b"helpers, changed\n")
-    assert bench.traffic_record("k") is None
+    assert bench.traffic_record("k", "C3") is None

@@ -57,7 +57,8 @@ def _small_case(Hq=8, Hkv=2, d=128, dtype=torch.bfloat16, fill=float("nan")):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (8, 1), (16, 8), (6, 3)])
-@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float16)])
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float16),
+                                     (64, torch.bfloat16), (128, torch.float16)])
 @pytest.mark.parametrize("ns", [1, 2, 3, 6])
 def test_decode_small_cases(bsa, Hq, Hkv, d, dtype, ns):
     q, k, v, sl, idx = _small_case(Hq, Hkv, d, dtype)
@@ -80,6 +81,37 @@ def test_decode_bad_index_is_skipped_and_flagged(bsa):
     assert bsa.bsattn_get_device_status(ws) & bsa.BSATTN_ERR_BAD_INDEX
     want = oracle.decode_varlen(q, k, v, sl, idx)
     assert _err(got, want) <= TOL[torch.bfloat16]
+
+
+def _poison_unselected(k, v, sl, idx):
+    """NaN in every valid token of a block that (b, kv head) does not select; the tokens
+    past cache_seqlens keep what they hold."""
+    B, Smax, Hkv, _ = k.shape
+    nb = (Smax + 63) // 64
+    sel = torch.zeros(B, Hkv, nb + 1, dtype=torch.bool)
+    ids = idx.long().clamp(min=-1)
+    sel.scatter_(2, torch.where(ids < 0, torch.full_like(ids, nb), ids), True)
+    tok = torch.arange(Smax)
+    valid = tok[None, :] < sl.long()[:, None]                        # [B, Smax]
+    chosen = sel[:, :, tok // 64].permute(0, 2, 1)                   # [B, Smax, Hkv]
+    poison = valid[:, :, None] & ~chosen
+    kp, vp = k.clone(), v.clone()
+    kp[poison] = float("nan")
+    vp[poison] = float("nan")
+    return kp, vp
+
+
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float16)])
+@pytest.mark.parametrize("ns", [1, 3])
+def test_decode_unselected_blocks_are_never_loaded(bsa, d, dtype, ns):
+    """Valid blocks that a (b, kv head) does not select hold NaN (so do the tokens past
+    cache_seqlens): the output matches the oracle on the clean cache bit for bit against the
+    clean run -- the selection decides which tiles are read, not only which are used."""
+    q, k, v, sl, idx = _small_case(8, 2, d, dtype)
+    kp, vp = _poison_unselected(k, v, sl, idx)
+    got = _run(bsa, q, kp, vp, sl, idx, ns)
+    assert torch.equal(got, _run(bsa, q, k, v, sl, idx, ns))
+    assert _err(got, oracle.decode_varlen(q, k, v, sl, idx)) <= TOL[dtype]
 
 
 @pytest.fixture(scope="module")
@@ -118,6 +150,15 @@ def test_decode_empty_selection_is_zero(bsa, c5):
     assert torch.count_nonzero(got[3]) == 0
     want = oracle.decode_varlen(q, k, v, sl, idx2)
     assert _err(got, want) <= TOL[cfg.dtype]
+
+
+def test_c5_unselected_blocks_are_never_loaded(bsa, c5):
+    """C5 at full size with NaN in every valid token of every unselected block."""
+    cfg, q, k, v, sl, idx, want = c5
+    kp, vp = _poison_unselected(k, v, sl, idx)
+    got = _run(bsa, q, kp, vp, sl, idx, 0)
+    assert _err(got, want) <= TOL[cfg.dtype]
+    assert torch.equal(got, _run(bsa, q, k, v, sl, idx, 0))
 
 
 def test_decode_is_deterministic(bsa, c5):
