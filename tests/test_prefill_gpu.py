@@ -188,10 +188,28 @@ def test_unselected_tiles_are_never_loaded_full_size(bsa, name):
     assert torch.equal(clean, poisoned)
 
 
-def test_timeout_path_reports_and_recovers(bsa):
+@pytest.mark.parametrize("d,dtype,causal", [(64, torch.float16, True), (64, torch.bfloat16, False),
+                                            (128, torch.bfloat16, True), (128, torch.float16, False)])
+def test_prefill_rescale_path(bsa, d, dtype, causal):
+    """Scores that grow by far more than 2^8 (in exp2 units) from one key block to the next:
+    the online softmax must rescale the accumulated output (the kernels do so lazily, only
+    past that growth), and the result still matches the oracle."""
+    B, H, S = 1, 3, 900
+    q, k, v = synthetic.qkv(B, H, S, S, d, dtype, seed=41 + d)
+    nb = math.ceil(S / 64)
+    scale = torch.tensor([4.0 * kb + 1.0 for kb in range(nb)]).repeat_interleave(64)[:S]
+    k = (k.float() * scale[None, None, :, None]).to(dtype)
+    mask = synthetic.random_block_mask(B, H, nb, nb, 0.6, seed=d)
+    got = _run(bsa, q, k, v, mask, causal)
+    want = oracle.prefill(q, k, v, mask, causal)
+    assert _err(got, want) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_timeout_path_reports_and_recovers(bsa, d):
     """A wait budget of 0 makes the kernels' bounded waits expire: the call must record
     BSATTN_ERR_TIMEOUT in the status word and leave the context usable."""
-    q, k, v = synthetic.qkv(2, 8, 2048, 2048, 128, torch.bfloat16, seed=4)
+    q, k, v = synthetic.qkv(2, 8, 2048, 2048, d, torch.bfloat16, seed=4)
     mask = synthetic.random_block_mask(2, 8, 32, 32, 0.5, seed=4)
     dev = torch.device("cuda")
     qd, kd, vd, md = q.to(dev), k.to(dev), v.to(dev), mask.to(dev)
