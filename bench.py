@@ -55,6 +55,8 @@ DESCRIBE = {
     "C3": "prefill B=1 H=32 S=16384 d=128 bf16 threshold-0.9+tril+dense-last causal",
     "C4": "prefill B=4 H=16 S=8192 d=64 fp16 threshold-0.75 non-causal",
     "C5": "GQA varlen sparse decode B=8 Hq=32 Hkv=8 d=128 bf16, 64 blocks/(b,kv-head)",
+    "C3/128": "prefill B=1 H=32 S=16384 d=128 bf16 threshold-0.9+tril+dense-last causal on 128-token "
+              "blocks (the 128-row kernel)",
 }
 TOL = {torch.float16: 1e-2, torch.bfloat16: 2e-2}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -242,12 +244,19 @@ def oracle_mask(scores, cfg):
     return oracle.mask_from_threshold(scores, cfg.param, cfg.dense_last, cfg.tril)
 
 
-def prefill_flops(mask, cfg):
-    nq = mask.shape[2]
-    keep = torch.ones(nq, mask.shape[3], dtype=torch.bool)
+def prefill_flops(mask, cfg, block=64):
+    """Effective FLOPs: 4*64*64*d per visited 64x64 tile pair (a 128-token entry stands for its
+    four tiles, of which the causal rule keeps those on or below the diagonal)."""
+    m = torch.as_tensor(mask) != 0
+    if block == 128:
+        m = m.repeat_interleave(2, dim=2).repeat_interleave(2, dim=3)
+        n = -(-cfg.S // 64)
+        m = m[:, :, :n, :n]
+    nq = m.shape[2]
+    keep = torch.ones(nq, m.shape[3], dtype=torch.bool)
     if cfg.causal:
         keep = keep.tril()
-    pairs = int(((torch.as_tensor(mask) != 0) & keep).sum())
+    pairs = int((m & keep).sum())
     return pairs * 4.0 * 64 * 64 * cfg.d, pairs
 
 
@@ -414,6 +423,23 @@ def run_gpu(args):
                              "value": round(ach, 2), "unit": "TFLOP/s",
                              "frac": round(ach / pk["bf16_tflops"], 4)}
             del cgq, cgk, cgv, cgm, cout
+        # the largest workload's shape and rule on 128-token blocks: the 128-row kernel
+        cfg = PREFILL
+        n128 = -(-cfg.S // 128)
+        scores128 = synthetic.block_scores(cfg.B, cfg.H, n128, n128, seed=0)
+        m128 = torch.as_tensor(library_mask(scores128, cfg))
+        cflops, cpairs = prefill_flops(m128, cfg, block=128)
+        gm128 = m128.to(dev)
+        cout = torch.empty_like(gq)
+        ms = time_calls(lambda: bsa.bsattn_prefill(gq, gk, gv, gm128, cfg.causal, out=cout,
+                                                   block_size=128), stream, cold_l2, reps)
+        outputs["C3/128"] = (cfg, q, k, v, m128, cout.cpu(), scores128)
+        ach = cflops / (ms / 1e3) / 1e12
+        per_cfg["C3/128"] = {"workload": DESCRIBE["C3/128"], "ms": round(ms, 4),
+                             "active_tile_pairs": cpairs, "gflop": round(cflops / 1e9, 3),
+                             "value": round(ach, 2), "unit": "TFLOP/s",
+                             "frac": round(ach / pk["bf16_tflops"], 4)}
+        del gm128, cout
         ms = time_calls(lambda: bsa.bsattn_decode_varlen(gdq, gdk, gdv, gsl, gidx, ns, out=dout),
                         stream, cold_l2, reps)
         ms_page = time_calls(lambda: bsa.bsattn_decode_varlen(gdq, gdk, gdv, gsl, gidx, ns_page,
@@ -537,6 +563,17 @@ def parity(outputs, per_cfg, decode_in):
                               "pass": err <= TOL[cfg.dtype] and same_mask,
                               "mask_bit_exact": same_mask, "oracle_s": round(t_or, 2)})
         res[name] = per_cfg[name]["pass"]
+    cfg, q, k, v, mask, got, scores128 = outputs["C3/128"]
+    want_mask = oracle_mask(scores128, cfg)
+    same_mask = bool(np.array_equal(np.asarray(mask), want_mask))
+    t0 = time.perf_counter()
+    want = oracle.prefill(q, k, v, want_mask, cfg.causal, block=128)
+    t_or = time.perf_counter() - t0
+    err = float(np.abs(got.double().numpy() - want).max())
+    per_cfg["C3/128"].update({"max_err": err, "tol": TOL[cfg.dtype],
+                              "pass": err <= TOL[cfg.dtype] and same_mask,
+                              "mask_bit_exact": same_mask, "oracle_s": round(t_or, 2)})
+    res["C3/128"] = per_cfg["C3/128"]["pass"]
     dq, dk, dv, sl, idx = decode_in
     t0 = time.perf_counter()
     want = oracle.decode_varlen(dq, dk, dv, sl, idx)

@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 namespace bsattn {
 
@@ -20,5 +21,11 @@ int encode_3d(CUtensorMap* map, const void* base, int bf16, uint64_t dim0, uint6
 int num_sms_of_current_device();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The 128-row prefill for a 128-token block mask (prefill128.cu).  Arguments are checked by the
+// caller; returns BSATTN_ERR_UNSUPPORTED when the mask rows do not fit its shared memory.
+int prefill128_launch(const void* q, const void* k, const void* v, const uint8_t* block_mask,
+                      int is_causal, void* out, int B, int H, int Sq, int Sk, int d, bool bf16,
+                      void* workspace, cudaStream_t stream);
 
 }  // namespace bsattn

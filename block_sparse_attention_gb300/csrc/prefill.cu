@@ -1187,6 +1187,13 @@ extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
     }
     const int nq = (Sq + 63) / 64, nk = (Sk + 63) / 64;
     if (nk > 4096 || BH * nq > 0x7fffffffLL || BH > 0x7fffffffLL) return BSATTN_ERR_UNSUPPORTED;
+    if (block_size == 128 && nk < kSplitMinNk) {
+        // both 64-row halves of a 128-token query block visit the same keys: full-rate M = 128
+        // tiles, unless the mask rows do not fit that kernel's shared memory
+        const int rc = prefill128_launch(q, k, v, block_mask, is_causal, out, B, H, Sq, Sk, d,
+                                         dtype == BSATTN_BF16, workspace, st);
+        if (rc != BSATTN_ERR_UNSUPPORTED) return rc;
+    }
     PrefillParams prm{};
     prm.mask = block_mask;
     prm.ws = static_cast<int*>(workspace);

@@ -277,16 +277,20 @@ BS128_CASES = [
     (1, 2, 128, 128, 64, torch.float16, True, 0.6),
     (2, 2, 300, 300, 128, torch.bfloat16, True, 0.5),
     (1, 2, 130, 400, 128, torch.bfloat16, True, 0.7),      # Sq < Sk, bottom-right causal
+    (1, 2, 400, 130, 64, torch.float16, True, 0.7),        # Sq > Sk: early rows see no key
     (1, 3, 700, 700, 64, torch.float16, False, 0.4),
     (1, 1, 1000, 1000, 128, torch.bfloat16, True, 1.0),
+    (2, 3, 1111, 1111, 128, torch.float16, False, 0.3),
+    (1, 1, 1, 1, 64, torch.bfloat16, True, 1.0),
+    (1, 2, 127, 129, 64, torch.bfloat16, False, 1.0),
 ]
 
 
 @pytest.mark.parametrize("B,H,Sq,Sk,d,dtype,causal,density", BS128_CASES)
 def test_prefill_block128(bsa, B, H, Sq, Sk, d, dtype, causal, density):
-    """128-token mask blocks: parity with the oracle at block 128, and bit-identical output to
-    the same mask expanded to 64-token blocks (the kernel visits the same tiles in the same
-    order either way)."""
+    """128-token mask blocks (the 128-row kernel, full-rate M = 128 tiles): parity with the
+    oracle at block 128, and agreement with the same mask expanded to 64-token blocks (the 64-row
+    kernel) within the tolerance; rows the oracle says are zero are exactly zero."""
     q, k, v = synthetic.qkv(B, H, Sq, Sk, d, dtype, seed=Sq + 3 * d)
     mask = synthetic.random_block_mask(B, H, math.ceil(Sq / 128), math.ceil(Sk / 128), density,
                                        seed=Sk + 1)
@@ -295,6 +299,71 @@ def test_prefill_block128(bsa, B, H, Sq, Sk, d, dtype, causal, density):
                              block_size=128).cpu()
     want = oracle.prefill(q, k, v, mask, causal, block=128)
     assert _err(got, want) <= TOL[dtype]
+    zero_rows = np.all(want == 0.0, axis=-1)
+    assert np.all(got.double().numpy()[zero_rows] == 0.0)
     m64 = mask.repeat_interleave(2, dim=2).repeat_interleave(2, dim=3)
     m64 = m64[:, :, :math.ceil(Sq / 64), :math.ceil(Sk / 64)].contiguous()
-    assert torch.equal(got, _run(bsa, q, k, v, m64, causal))
+    assert float((got.float() - _run(bsa, q, k, v, m64, causal).float()).abs().max()) <= TOL[dtype]
+
+
+def _block128_workload(name):
+    """A full workload's shape and mask rule on 128-token blocks (scores [B, H, S/128, S/128])."""
+    cfg = synthetic.PREFILL_CONFIGS[name]
+    q, k, v, _ = synthetic.prefill_inputs(cfg)
+    n = math.ceil(cfg.S / 128)
+    scores = synthetic.block_scores(cfg.B, cfg.H, n, n, seed=0)
+    return cfg, q, k, v, torch.as_tensor(_workload_mask(cfg, scores))
+
+
+@pytest.mark.parametrize("name", ["C3", "C4"])
+def test_block128_full_size_every_element(bsa, name):
+    """C3 and C4 shapes with their mask rules on 128-token blocks, through the 128-row kernel,
+    against the oracle on every output element."""
+    cfg, q, k, v, mask = _block128_workload(name)
+    dev = torch.device("cuda")
+    got = bsa.bsattn_prefill(q.to(dev), k.to(dev), v.to(dev), mask.to(dev), cfg.causal,
+                             block_size=128).cpu()
+    want = oracle.prefill(q, k, v, mask, cfg.causal, block=128)
+    assert torch.isfinite(got.float()).all()
+    assert _err(got, want) <= TOL[cfg.dtype]
+
+
+@pytest.mark.parametrize("d,dtype,causal", [(128, torch.bfloat16, True), (64, torch.float16, False)])
+def test_block128_unselected_tiles_are_never_loaded(bsa, d, dtype, causal):
+    """The 128-row kernel skips unselected blocks without loading them: NaN in every K/V block
+    no visited 128-token entry selects leaves the output bit-identical to the clean run."""
+    B, H, S = 1, 3, 1700
+    q, k, v = synthetic.qkv(B, H, S, S, d, dtype, seed=51 + d)
+    nb = math.ceil(S / 128)
+    mask, used = _used_columns_mask(B, H, nb, nb, 0.5, seed=d + 1, causal=causal)
+    used64 = used.repeat_interleave(2, dim=2)[:, :, :math.ceil(S / 64)]
+    kp, vp = _poison_unused(k, v, used64)
+    dev = torch.device("cuda")
+    run = lambda kk, vv: bsa.bsattn_prefill(q.to(dev), kk.to(dev), vv.to(dev), mask.to(dev), causal,
+                                            block_size=128).cpu()
+    clean, poisoned = run(k, v), run(kp, vp)
+    assert torch.equal(clean, poisoned)
+    assert _err(poisoned, oracle.prefill(q, k, v, mask, causal, block=128)) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_block128_timeout_path_reports_and_recovers(bsa, d):
+    """The 128-row kernel's bounded waits expire with a budget of 0: BSATTN_ERR_TIMEOUT is
+    recorded and the next call is correct."""
+    q, k, v = synthetic.qkv(2, 8, 2048, 2048, d, torch.bfloat16, seed=6)
+    mask = synthetic.random_block_mask(2, 8, 16, 16, 0.5, seed=6)
+    dev = torch.device("cuda")
+    qd, kd, vd, md = q.to(dev), k.to(dev), v.to(dev), mask.to(dev)
+    ws = bsa.workspace(dev, "prefill", 256)
+    bsa.bsattn_get_device_status(ws)
+    try:
+        bsa.bsattn_set_wait_budget_ns(0)
+        bsa.bsattn_prefill(qd, kd, vd, md, True, block_size=128)
+        torch.cuda.synchronize()
+    finally:
+        bsa.bsattn_set_wait_budget_ns(2_000_000_000)
+    assert bsa.bsattn_get_device_status(ws) & bsa.BSATTN_ERR_TIMEOUT
+    got = bsa.bsattn_prefill(qd, kd, vd, md, True, block_size=128).cpu()
+    assert bsa.bsattn_get_device_status(ws) == 0
+    want = oracle.prefill(q[:1, :2], k[:1, :2], v[:1, :2], mask[:1, :2], True, block=128)
+    assert _err(got[:1, :2], want) <= TOL[torch.bfloat16]
