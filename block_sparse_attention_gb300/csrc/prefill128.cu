@@ -23,10 +23,13 @@
 //   warps 0-3   softmax: thread t of warp w owns query row 32 w + t.  A tile's 64 scores are read
 //               from TMEM in two passes of 32 so that 32 are live at a time (the second half for
 //               its maximum, then the first half, then the second half again).
-// TMEM: S[0] columns 0-63, S[1] 64-127, O 128-(128+d).  Shared memory: Q, three K and three V
-// stages and two P tiles of [128 x 64]: 96 KB at d = 64 (two CTAs per SM), 160 KB at d = 128 (one
-// CTA per SM).  Every wait is bounded: on expiry the CTA records BSATTN_ERR_TIMEOUT, drains the
-// copies and MMAs in flight, frees its TMEM and exits.
+// TMEM: S[0] columns 0-63, S[1] 64-127, O 128-(128+d).  Shared memory (see Cfg): at d = 64 Q,
+// three K and three V stages and two P tiles of [128 x 64] (96 KB, two CTAs per SM); at d = 128,
+// for masks up to 256 key tiles wide, Q, two K and two V stages and one P tile (112.6 KB, two CTAs
+// per SM: two softmax pipelines per SM made the C3-shaped 128-token workload 1.55x faster than one
+// CTA per SM with deeper rings), else three stages each and two P tiles (160 KB, one CTA per SM).
+// Every wait is bounded: on expiry the CTA records BSATTN_ERR_TIMEOUT, drains the copies and MMAs
+// in flight, frees its TMEM and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -44,10 +47,6 @@ constexpr int kSWarp = 4;               // issues Q K^T, owns TMEM
 constexpr int kProdWarp = 5;            // TMA producer
 constexpr int kPVWarp = 6;              // issues P V
 constexpr int kSchedWarp = 7;           // fetches items, compacts their mask rows
-constexpr int kKS = 3;                  // K stages
-constexpr int kVS = 3;                  // V stages
-constexpr int kPT = 2;                  // P tiles
-constexpr int kSlots = 3;               // items published ahead of the consumers
 constexpr uint32_t kTmemCols = 256;     // S[0] 0-63, S[1] 64-127, O 128-(128+d)
 constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
@@ -56,9 +55,22 @@ constexpr int kWsStatus = 0;
 constexpr int kWsNext = 16;
 constexpr int kWsDone = 32;
 
-template <int D>
+// Shared-memory configurations.  Wide: Q, three K and three V stages, two P tiles, three item
+// slots with 16-bit tile lists; at d = 64 two CTAs per SM (96 KB), at d = 128 one (160 KB).
+// Narrow (d = 128 only, masks up to 256 key tiles): Q, two K and two V stages, one P tile, two
+// item slots with 8-bit tile lists, laid out from the dynamic shared memory base itself (which
+// the kernel checks is 1024-byte aligned) -- 112.6 KB, so that two CTAs share an SM.
+template <int D, bool NARROW = false>
 struct Cfg {
-    static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+    static_assert(!NARROW || D == 128, "the narrow configuration is for d = 128");
+    static constexpr int kKS = NARROW ? 2 : 3;          // K stages
+    static constexpr int kVS = NARROW ? 2 : 3;          // V stages
+    static constexpr int kPT = NARROW ? 1 : 2;          // P tiles
+    static constexpr int kSlots = NARROW ? 2 : 3;       // items published ahead of the consumers
+    using ListT = std::conditional_t<NARROW, uint8_t, uint16_t>;
+    static constexpr int kMaxNk = NARROW ? 256 : 65535;
+    static constexpr uint32_t kSlack = NARROW ? 0 : 1024;   // room to align the base up
+    static constexpr int kCtasPerSm = (D == 64 || NARROW) ? 2 : 1;
     static constexpr uint32_t kKTile = (D / 64) * 8192;     // [64 keys x D] 16-bit
     static constexpr uint32_t kQTile = (D / 64) * 16384;    // [128 rows x D]
     static constexpr uint32_t kPTile = 16384;               // [128 rows x 64 keys]
@@ -72,9 +84,11 @@ struct Cfg {
     static constexpr uint32_t kNumBars = 2 + 2 * kKS + 2 * kVS + 4 + 2 * kPT + 1 + 2 * kSlots + 3;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, then 4 ints per slot
     static constexpr uint32_t kList = kMisc + 16 + 16 * kSlots;
-    static constexpr uint32_t kSmemMax = D == 64 ? 113u * 1024u : 227u * 1024u;
-    __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
-    static uint32_t bytes(int nk) { return 1024 + kList + kSlots * list_stride(nk); }
+    static constexpr uint32_t kSmemMax = kCtasPerSm == 2 ? 113u * 1024u : 227u * 1024u;
+    __host__ __device__ static uint32_t list_stride(int nk) {
+        return (static_cast<uint32_t>(sizeof(ListT)) * nk + 15) & ~15u;
+    }
+    static uint32_t bytes(int nk) { return kSlack + kList + kSlots * list_stride(nk); }
 };
 
 struct Params128 {
@@ -180,13 +194,30 @@ __device__ __forceinline__ void decode_item(int t, int BH, int nq, int win, int&
     bh = h0 + (r - (r / wh) * wh);
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
+template <int D, bool BF16, bool NARROW>
+__global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
     prefill128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Params128 p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, NARROW>;
     using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
+    using ListT = typename C::ListT;
+    constexpr int kKS = C::kKS, kVS = C::kVS, kPT = C::kPT, kSlots = C::kSlots;
     extern __shared__ uint8_t smem_raw[];
+    if constexpr (NARROW) {
+        // this layout has no slack to align the base up: every CTA leaves (counted as finished)
+        // with an error if the base is not 1024-byte aligned
+        if (smem_u32(smem_raw) & 1023u) {
+            if (threadIdx.x == 0) {
+                atomicOr(p.ws + kWsStatus, BSATTN_ERR_CUDA);
+                __threadfence();
+                if (atomicAdd(p.ws + kWsDone, 1) == static_cast<int>(gridDim.x) - 1) {
+                    atomicExch(p.ws + kWsNext, 0);
+                    atomicExch(p.ws + kWsDone, 0);
+                }
+            }
+            return;
+        }
+    }
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
     uint8_t* sq = sm + C::kQ;
@@ -216,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
     int* bh_of = count_of + kSlots;                      // [slots]
     int* qb_of = bh_of + kSlots;                         // [slots]
     const uint32_t lstride = C::list_stride(p.nk);
-    uint16_t* lists = reinterpret_cast<uint16_t*>(sm + C::kList);
+    ListT* lists = reinterpret_cast<ListT*>(sm + C::kList);
     volatile int* abort_flag = &misc[1];
     int* status = p.ws + kWsStatus;
 
@@ -311,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
             // compact the mask row into the visited 64-key tiles, ascending: tile kb reads
             // entry kb / 2 of the row
             const uint8_t* mrow = p.mask + (static_cast<size_t>(bh) * p.nq + qb) * p.mk;
-            uint16_t* list = lists + slot * (lstride / 2);
+            ListT* list = lists + slot * (lstride / sizeof(ListT));
             int count = 0;
             for (int base = 0; base < kb_end; base += 256) {
                 uint32_t bits = 0;
@@ -325,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
                     const int kb = base + 32 * u + lane;
                     const bool on = (bits >> u) & 1u;
                     const uint32_t ballot = __ballot_sync(0xffffffffu, on);
-                    if (on) list[count + __popc(ballot & ((1u << lane) - 1u))] = static_cast<uint16_t>(kb);
+                    if (on) list[count + __popc(ballot & ((1u << lane) - 1u))] = static_cast<ListT>(kb);
                     count += __popc(ballot);
                 }
             }
@@ -361,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
                 if (t < 0) break;
                 if (count > 0) {
                     const int bh = bh_of[slot], qb = qb_of[slot];
-                    const uint16_t* list = lists + slot * (lstride / 2);
+                    const ListT* list = lists + slot * (lstride / sizeof(ListT));
                     if (kside) {
                         // the previous item's Q K^T must be done before its Q is overwritten
                         if (qloads >= 1 && !wait_parity(q_free, (qloads - 1) & 1, deadline, abort_flag, status)) {
@@ -525,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
             const int cnt = count_of[slot];
             if (item < 0) break;
             const int bh = bh_of[slot], qb = qb_of[slot];
-            const uint16_t* list = lists + slot * (lstride / 2);
+            const ListT* list = lists + slot * (lstride / sizeof(ListT));
             if (cnt == 0) {
                 // no visible key anywhere in this query block: its rows are exactly zero
                 const int rows = min(128, p.Sq - qb * 128);
@@ -538,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
                 continue;
             }
             const int row = qb * 128 + lrow;
+            // keys at or past `lim` are not visible to this row (sequence end; causal diagonal)
+            const int lim = p.causal ? min(p.Sk, row + past + 1) : p.Sk;
             float m_used = -INFINITY;
             float l = 0.f;
             bool ok = true;
@@ -550,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
                 }
                 tc_fence_after();
                 const int key0 = static_cast<int>(list[i]) * 64;
-                const bool edge = key0 + 63 >= p.Sk || (p.causal && key0 + 63 > row + past);
+                const bool edge = key0 + 63 >= lim;
                 // 32 scores of half h of the tile, masked on the diagonal / sequence tail
                 auto load_half = [&](int h, float (&sc)[32]) {
                     uint32_t r[32];
@@ -559,10 +592,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) sc[e] = __uint_as_float(r[e]);
                     if (edge) {
-                        const int kh = key0 + 32 * h;
+                        const int n = lim - (key0 + 32 * h);          // visible scores of this half
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (kh + e >= p.Sk || (p.causal && kh + e > row + past)) sc[e] = -INFINITY;
+                            if (e >= n) sc[e] = -INFINITY;
                     }
                 };
                 auto max32 = [&](const float (&sc)[32]) -> float {
@@ -655,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + row) * D);
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld_row32(tl + kOCol + c0, o);
@@ -699,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kCtasPerSm)
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool NARROW = false>
 int launch128(const void* q, const void* k, const void* v, const Params128& prm, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, NARROW>;
     const uint32_t smem = C::bytes(prm.nk);
-    if (smem > C::kSmemMax) return BSATTN_ERR_UNSUPPORTED;
+    if (smem > C::kSmemMax || prm.nk > C::kMaxNk) return BSATTN_ERR_UNSUPPORTED;
     CUtensorMap tq, tk, tv;
     const uint64_t BH = static_cast<uint64_t>(prm.B) * prm.H;
     int rc = 0;
@@ -711,7 +744,7 @@ int launch128(const void* q, const void* k, const void* v, const Params128& prm,
     rc |= encode_3d(&tk, k, BF16, D, prm.Sk, BH, D * 2ull, uint64_t(prm.Sk) * D * 2, 64, 64, 1, true);
     rc |= encode_3d(&tv, v, BF16, D, prm.Sk, BH, D * 2ull, uint64_t(prm.Sk) * D * 2, 64, 64, 1, true);
     if (rc) return rc;
-    auto kern = prefill128_kernel<D, BF16>;
+    auto kern = prefill128_kernel<D, BF16, NARROW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSATTN_ERR_CUDA;
     int sms = num_sms_of_current_device();
@@ -747,7 +780,13 @@ int prefill128_launch(const void* q, const void* k, const void* v, const uint8_t
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.budget_ns = wait_budget_ns();
     if (d == 64) return bf16 ? launch128<64, true>(q, k, v, prm, stream) : launch128<64, false>(q, k, v, prm, stream);
-    if (d == 128) return bf16 ? launch128<128, true>(q, k, v, prm, stream) : launch128<128, false>(q, k, v, prm, stream);
+    if (d == 128) {
+        // two CTAs per SM (the narrow layout) whenever the mask rows allow it
+        if (prm.nk <= Cfg<128, true>::kMaxNk && Cfg<128, true>::bytes(prm.nk) <= Cfg<128, true>::kSmemMax)
+            return bf16 ? launch128<128, true, true>(q, k, v, prm, stream)
+                        : launch128<128, false, true>(q, k, v, prm, stream);
+        return bf16 ? launch128<128, true>(q, k, v, prm, stream) : launch128<128, false>(q, k, v, prm, stream);
+    }
     return BSATTN_ERR_UNSUPPORTED;
 }
 

@@ -283,6 +283,8 @@ BS128_CASES = [
     (2, 3, 1111, 1111, 128, torch.float16, False, 0.3),
     (1, 1, 1, 1, 64, torch.bfloat16, True, 1.0),
     (1, 2, 127, 129, 64, torch.bfloat16, False, 1.0),
+    # more than 256 key tiles at d = 128: the one-CTA-per-SM layout
+    (1, 2, 20000, 20000, 128, torch.bfloat16, True, 0.08),
 ]
 
 
