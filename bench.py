@@ -286,6 +286,42 @@ class L2Flush:
         self.clean.max()
 
 
+def pipelined(n, host_in, dev_in, compute, dev_out, host_out, dev):
+    """Runs n steps, each copying `host_in` (pinned) into device buffer set i % 2, computing into
+    dev_out[i % 2] and copying that back into host_out[i % 2], on three streams so that the
+    copies of one step overlap the computation of its neighbours.  Returns the elapsed ms from
+    the first input copy to the last output copy (CUDA events)."""
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(s_in)
+    for i in range(n):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_cmp[b])         # step i-2 no longer reads buffer set b
+            for d, h in zip(dev_in[b], host_in):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[b])
+            if i >= 2:
+                s_cmp.wait_event(ev_out[b])        # step i-2's output has left dev_out[b]
+            compute(b)
+            ev_cmp[b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[b])
+            host_out[b].copy_(dev_out[b], non_blocking=True)
+            ev_out[b].record(s_out)
+    s_out.wait_event(ev_in[(n - 1) % 2])
+    end.record(s_out)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
 def time_calls(fn, stream, flush, reps, warm=3):
     """Median CUDA-event time (ms) of fn(), each call after an L2 flush outside the events."""
     for i in range(warm):
@@ -363,40 +399,51 @@ def run_gpu(args):
     status = bsa.bsattn_get_device_status(bsa.workspace(dev, "prefill", 256)) | \
         bsa.bsattn_get_device_status(bsa.workspace(dev, "decode", 256))
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed
+    # ---- end to end through the public API with host buffers (pinned), copies timed: every step
+    # copies its inputs in and its output back; steps are pipelined over three streams (inputs of
+    # step i+1 in, step i computing, output of step i-1 out), with two device buffer sets
     hp = [t.pin_memory() for t in (q, k, v, mask)]
-    hdq, hsl, hidx = (t.pin_memory() for t in (dq, sl, idx))
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
-    dq_dev, sl_dev, idx_dev = torch.empty_like(gdq), torch.empty_like(gsl), torch.empty_like(gidx)
+    hdec = [t.pin_memory() for t in (dq, sl, idx)]
+    houts = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    hdouts = [torch.empty(dout.shape, dtype=dout.dtype).pin_memory() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 50))
     h2d_pre = sum(t.numel() * t.element_size() for t in hp)
-    h2d_dec = sum(t.numel() * t.element_size() for t in (hdq, hsl, hidx))
-    d2h_pre, d2h_dec = hout.numel() * 2, hdout.numel() * 2
-    e_pre, e_dec = [], []
+    h2d_dec = sum(t.numel() * t.element_size() for t in hdec)
+    d2h_pre, d2h_dec = out.numel() * 2, dout.numel() * 2
+    pin = [[torch.empty_like(t, device=dev) for t in hp] for _ in range(2)]
+    pout = [out, torch.empty_like(out)]
+    din = [[torch.empty_like(t, device=dev) for t in hdec] for _ in range(2)]
+    dpout = [dout, torch.empty_like(dout)]
+
+    def prefill_step(b):
+        tq, tk, tv, tm = pin[b]
+        bsa.bsattn_prefill(tq, tk, tv, tm, PREFILL.causal, out=pout[b])
+
+    def decode_step(b):
+        tq, tsl, tidx = din[b]
+        bsa.bsattn_decode_varlen(tq, gdk, gdv, tsl, tidx, ns, out=dpout[b])
+
     t_e0 = time.perf_counter()
+    pipelined(3, hp, pin, prefill_step, pout, houts, dev)             # warm-up
+    e_pre_ms = pipelined(e2e_steps, hp, pin, prefill_step, pout, houts, dev)
+    # the decode's copies are a few KB: a serial step (copies, kernel, copy back) beats the
+    # cross-stream events of the pipeline
+    e_dec_ms = 0.0
     for i in range(e2e_steps + 2):
-        cold_l2(i)
-        a, bq, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        tq, tk, tv, tm = (t.to(dev, non_blocking=True) for t in hp)
-        bsa.bsattn_prefill(tq, tk, tv, tm, PREFILL.causal, out=out)
-        hout.copy_(out, non_blocking=True)
-        bq.record(stream)
-        dq_dev.copy_(hdq, non_blocking=True)
-        sl_dev.copy_(hsl, non_blocking=True)
-        idx_dev.copy_(hidx, non_blocking=True)
-        bsa.bsattn_decode_varlen(dq_dev, gdk, gdv, sl_dev, idx_dev, ns, out=dout)
-        hdout.copy_(dout, non_blocking=True)
+        for d, h in zip(din[0], hdec):
+            d.copy_(h, non_blocking=True)
+        decode_step(0)
+        hdouts[0].copy_(dpout[0], non_blocking=True)
         c.record(stream)
         torch.cuda.synchronize()
         if i >= 2:
-            e_pre.append(a.elapsed_time(bq))
-            e_dec.append(bq.elapsed_time(c))
+            e_dec_ms += a.elapsed_time(c)
     clocks.phase("e2e", t_e0, time.perf_counter())
-    e_pre_s = max_over_ranks(sum(e_pre) / 1e3, world, dev)
-    e_dec_s = max_over_ranks(sum(e_dec) / 1e3, world, dev)
-    del tq, tk, tv, tm, hp
+    e_pre_s = max_over_ranks(e_pre_ms / 1e3, world, dev)
+    e_dec_s = max_over_ranks(e_dec_ms / 1e3, world, dev)
+    del pin, din, hp
 
     # ---- every workload of the set on its own (rank 0), plus a copy as long as the decode's
     per_cfg, outputs = {}, {}
@@ -526,11 +573,17 @@ def run_gpu(args):
         "prefill_ms_per_launch": round(per_launch_pre * 1e3, 4),
         "e2e": {"value": round(aggregate(flops, e2e_steps, world, e_pre_s) / 1e12, 3),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d_pre),
-                "d2h_bytes_per_step": int(d2h_pre),
+                "d2h_bytes_per_step": int(d2h_pre), "steps": e2e_steps,
+                "h2d_GBps": round(h2d_pre * e2e_steps / e_pre_s / 1e9, 1),
+                "note": "every step copies Q/K/V/mask in from pinned host memory and the output "
+                        "back; steps pipelined over three streams with two device buffer sets; "
+                        "L2 not flushed",
                 "decode": {"value": round(aggregate(dbytes, e2e_steps, world, e_dec_s) / 1e9, 1),
                            "unit": "GB/s", "h2d_bytes_per_step": int(h2d_dec),
                            "d2h_bytes_per_step": int(d2h_dec),
-                           "note": "KV cache device-resident across decode steps"}},
+                           "note": "q, cache_seqlens and block_indices in, the output back, one "
+                                   "step at a time; KV cache device-resident across decode "
+                                   "steps"}},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "device_status": status,
