@@ -671,10 +671,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
                 const int vs = g % kVStages;
-                if (!warp_wait_parity(&p_full[g % kPF], (g / kPF) & 1, deadline, abort_flag, status) ||
+                // V has usually landed long before P is written: polling v_full first leaves
+                // p_full the last wait before the issue
+                if (!warp_wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status) ||
                     (i == 0 && items >= 1 &&
                      !warp_wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status)) ||
-                    !warp_wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status)) {
+                    !warp_wait_parity(&p_full[g % kPF], (g / kPF) & 1, deadline, abort_flag, status)) {
                     ok = false;
                     break;
                 }

@@ -9,7 +9,8 @@
 //                   tiles), fp32 in TMEM
 //     token mask on the diagonal / sequence tail
 //     exp2 online softmax, one thread per query row (TMEM lane = row: no partner-lane shuffles)
-//     O += P V      tcgen05.mma M=128 N=d K=64, P rounded to the input type
+//     O += P V      tcgen05.mma M=128 N=d K=64 with A = P in TMEM (rounded to the input type and
+//                   written over its own S buffer, as the scores are already in registers)
 // and finally O / l (a row with no visible key stores exactly 0).
 //
 // Persistent kernel, 256 threads, the warp roles of the 64-row kernel:
@@ -17,19 +18,17 @@
 //               every head first, then windows of heads whose K and V fit in 32 MB), compacts the
 //               item's mask row into a list of 64-key tiles, publishes it;
 //   warp 5      producers: lane 0 loads Q (128 rows) and streams K tiles, lane 1 streams V tiles,
-//               three stages each, every stage released by the MMA commit that last reads it;
-//   warp 4      allocates TMEM and issues Q K^T into S[g % 2];
-//   warp 6      issues P V from P tile g % 2 into O;
+//               every stage released by the MMA commit that last reads it;
+//   warp 4      allocates TMEM and issues Q K^T into S[g % 2] once P V of block g - 2 (whose P
+//               sat in that buffer) is done;
+//   warp 6      issues P V with A = P from TMEM (S buffer g % 2) into O;
 //   warps 0-3   softmax: thread t of warp w owns query row 32 w + t.  A tile's 64 scores are read
 //               from TMEM in two passes of 32 so that 32 are live at a time (the second half for
 //               its maximum, then the first half, then the second half again).
-// TMEM: S[0] columns 0-63, S[1] 64-127, O 128-(128+d).  Shared memory (see Cfg): at d = 64 Q,
-// three K and three V stages and two P tiles of [128 x 64] (96 KB, two CTAs per SM); at d = 128,
-// for masks up to 256 key tiles wide, Q, two K and two V stages and one P tile (112.6 KB, two CTAs
-// per SM: two softmax pipelines per SM made the C3-shaped 128-token workload 1.55x faster than one
-// CTA per SM with deeper rings), else three stages each and two P tiles (160 KB, one CTA per SM).
-// Every wait is bounded: on expiry the CTA records BSATTN_ERR_TIMEOUT, drains the copies and MMAs
-// in flight, frees its TMEM and exits.
+// TMEM: S / P buffers at columns 0-63 and 64-127, O at 128-(128+d).  Shared memory holds only Q
+// and the K and V rings (see Cfg): P never leaves TMEM, so the softmax neither waits for a P tile
+// to free nor fences shared-memory writes before P V.  Every wait is bounded: on expiry the CTA
+// records BSATTN_ERR_TIMEOUT, drains the copies and MMAs in flight, frees its TMEM and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -55,17 +54,18 @@ constexpr int kWsStatus = 0;
 constexpr int kWsNext = 16;
 constexpr int kWsDone = 32;
 
-// Shared-memory configurations.  Wide: Q, three K and three V stages, two P tiles, three item
-// slots with 16-bit tile lists; at d = 64 two CTAs per SM (96 KB), at d = 128 one (160 KB).
-// Narrow (d = 128 only, masks up to 256 key tiles): Q, two K and two V stages, one P tile, two
-// item slots with 8-bit tile lists, laid out from the dynamic shared memory base itself (which
-// the kernel checks is 1024-byte aligned) -- 112.6 KB, so that two CTAs share an SM.
+// Shared-memory configurations (P lives in TMEM, so only Q and the K / V rings are here).
+// d = 64: Q, four K and four V stages, three item slots with 16-bit tile lists: 80 KB, two CTAs
+// per SM.  d = 128, masks up to 256 key tiles (narrow): Q, three K and two V stages, two item
+// slots with 8-bit tile lists, laid out from the dynamic shared memory base itself (which the
+// kernel checks is 1024-byte aligned): 112.8 KB, so that two CTAs share an SM.  d = 128, wider
+// masks: Q, three K and three V stages, three slots, 16-bit lists: 129 KB, one CTA per SM.
 template <int D, bool NARROW = false>
 struct Cfg {
     static_assert(!NARROW || D == 128, "the narrow configuration is for d = 128");
-    static constexpr int kKS = NARROW ? 2 : 3;          // K stages
-    static constexpr int kVS = NARROW ? 2 : 3;          // V stages
-    static constexpr int kPT = NARROW ? 1 : 2;          // P tiles
+    static constexpr int kKS = D == 64 ? 4 : 3;         // K stages
+    static constexpr int kVS = D == 64 ? 4 : (NARROW ? 2 : 3);   // V stages
+    static constexpr int kPT = 2;                       // S / P buffers in TMEM
     static constexpr int kSlots = NARROW ? 2 : 3;       // items published ahead of the consumers
     using ListT = std::conditional_t<NARROW, uint8_t, uint16_t>;
     static constexpr int kMaxNk = NARROW ? 256 : 65535;
@@ -73,12 +73,10 @@ struct Cfg {
     static constexpr int kCtasPerSm = (D == 64 || NARROW) ? 2 : 1;
     static constexpr uint32_t kKTile = (D / 64) * 8192;     // [64 keys x D] 16-bit
     static constexpr uint32_t kQTile = (D / 64) * 16384;    // [128 rows x D]
-    static constexpr uint32_t kPTile = 16384;               // [128 rows x 64 keys]
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + kQTile;
     static constexpr uint32_t kV = kK + kKS * kKTile;
-    static constexpr uint32_t kP = kV + kVS * kKTile;
-    static constexpr uint32_t kBars = kP + kPT * kPTile;
+    static constexpr uint32_t kBars = kV + kVS * kKTile;
     // q_full q_free k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] s_free[2]
     // p_full[PT] o_done[PT] o_free item_full[slots] item_empty[slots] loaded fin_s fin_pv
     static constexpr uint32_t kNumBars = 2 + 2 * kKS + 2 * kVS + 4 + 2 * kPT + 1 + 2 * kSlots + 3;
@@ -173,6 +171,31 @@ __device__ __forceinline__ void tmem_st_row32(uint32_t taddr, const uint32_t (&r
         : "memory");
 }
 
+// 32 TMEM lanes x 16 columns store: thread t writes lane (quarter base + t), columns [col, col + 16).
+__device__ __forceinline__ void tmem_st_row16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16, issued by one lane of a converged warp under a guard
+// predicate.  A (M = 128 rows x K = 16) sits in 128 TMEM lanes x 8 columns, two 16-bit values
+// per column, lower K index in the low half.
+__device__ __forceinline__ void mma_f16_ts_if(bool lead, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(lead ? 1u : 0u)
+        : "memory");
+}
+
 // Item t -> (bh, qb): the first min(2, nq) * BH items are the last two query blocks of every head
 // (under a causal mask they visit the most keys), then window by window, `win` heads at a time,
 // from the last query block to the first across the window's heads.
@@ -202,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
     using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
     using ListT = typename C::ListT;
     constexpr int kKS = C::kKS, kVS = C::kVS, kPT = C::kPT, kSlots = C::kSlots;
+    // TMEM columns: S buffers 0-63 and 64-127 (narrow: P of block g written over the first 32
+    // columns of its own S buffer once the scores are in registers), O from 128
     extern __shared__ uint8_t smem_raw[];
     if constexpr (NARROW) {
         // this layout has no slack to align the base up: every CTA leaves (counted as finished)
@@ -223,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
     uint8_t* sq = sm + C::kQ;
     uint8_t* sk = sm + C::kK;
     uint8_t* sv = sm + C::kV;
-    uint8_t* sp = sm + C::kP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
     uint64_t* q_full = bars;
     uint64_t* q_free = q_full + 1;
@@ -231,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
     uint64_t* k_empty = k_full + kKS;     // [KS]
     uint64_t* v_full = k_empty + kKS;     // [VS]
     uint64_t* v_empty = v_full + kVS;     // [VS]
-    uint64_t* s_full = v_empty + kVS;     // [2]
+    uint64_t* s_full = v_empty + kVS;     // [2] (one used when narrow)
     uint64_t* s_free = s_full + 2;        // [2]
     uint64_t* p_full = s_free + 2;        // [PT]
     uint64_t* o_done = p_full + kPT;      // [PT] P V of block g done (index g % PT)
@@ -269,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&s_full[j], 1);
-            mbar_init(&s_free[j], 4);                  // one arrival per softmax warp
+            mbar_init(&s_free[j], 1);                  // P V of the block (P sits in the buffer)
         }
         for (int j = 0; j < kPT; ++j) {
             mbar_init(&p_full[j], 4);
@@ -467,8 +491,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                 for (int i = 0; i < cnt; ++i) {
                     const int g = blk + i;
                     const int ks = g % kKS;
+                    const int sb = g & 1;
                     if (!warp_wait_parity(&k_full[ks], (g / kKS) & 1, deadline, abort_flag, status) ||
-                        (g >= 2 && !warp_wait_parity(&s_free[g & 1], ((g - 2) >> 1) & 1, deadline, abort_flag,
+                        (g >= 2 && !warp_wait_parity(&s_free[sb], ((g - 2) >> 1) & 1, deadline, abort_flag,
                                                      status))) {
                         ok = false;
                         break;
@@ -481,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t a_off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                         const uint32_t b_off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                        mma_f16_ss_if(lead, tbase + (g & 1) * 64, a_base + a_off, b_stage + b_off, idS,
+                        mma_f16_ss_if(lead, tbase + sb * 64, a_base + a_off, b_stage + b_off, idS,
                                       kk > 0 ? 1u : 0u);
                     }
-                    mma_commit_if(lead, &s_full[g & 1]);
+                    mma_commit_if(lead, &s_full[sb]);
                     mma_commit_if(lead, &k_empty[ks]);                 // K stage free
                     if (i == cnt - 1) mma_commit_if(lead, q_free);     // Q no longer read
                 }
@@ -501,7 +526,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
         // ------------------------------------------------------------ P V issuer
         const bool lead = lane == 0;
         constexpr uint32_t idO = idesc_f16(128, D, BF16, true);
-        const uint64_t p_desc = sdesc_sw128(smem_u32(sp), 16, 1024);
         const uint64_t v_desc = sdesc_sw128(smem_u32(sv), 8192, 1024);
         int blk = 0, items = 0;
         for (int n = 0;; ++n) {
@@ -514,22 +538,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
                 const int vs = g % kVS;
-                if (!warp_wait_parity(&p_full[g % kPT], (g / kPT) & 1, deadline, abort_flag, status) ||
+                // V has usually landed long before P is written: polling v_full first leaves
+                // p_full the last wait before the issue
+                if (!warp_wait_parity(&v_full[vs], (g / kVS) & 1, deadline, abort_flag, status) ||
                     (i == 0 && items >= 1 &&
                      !warp_wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status)) ||
-                    !warp_wait_parity(&v_full[vs], (g / kVS) & 1, deadline, abort_flag, status)) {
+                    !warp_wait_parity(&p_full[g % kPT], (g / kPT) & 1, deadline, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 // 16 keys of P are 32 bytes along its rows; 16 tokens of V are 16 rows of 128 bytes
-                const uint64_t a0 = p_desc + static_cast<uint32_t>(g % kPT) * (C::kPTile >> 4);
                 const uint64_t b0 = v_desc + static_cast<uint32_t>(vs) * (C::kKTile >> 4);
+                // A = P of block g in TMEM, over the first 32 columns of S buffer g % 2: 16 keys
+                // are 8 columns
+                const uint32_t a0 = tbase + 64 * (g & 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f16_ss_if(lead, tbase + kOCol, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO,
+                    mma_f16_ts_if(lead, tbase + kOCol, a0 + 8 * kk, b0 + ((kk * 2048) >> 4), idO,
                                   (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_if(lead, &o_done[g % kPT]);   // P V of g done: O holds it, its P tile is free
+                mma_commit_if(lead, &o_done[g % kPT]);   // P V of g done: O holds it
+                mma_commit_if(lead, &s_free[g & 1]);     // S / P buffer g % 2 free for Q K^T of g + 2
                 mma_commit_if(lead, &v_empty[vs]);       // V stage free
             }
             if (!ok) break;
@@ -620,40 +649,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                 const bool rescale_o = grow && m_used != -INFINITY;
                 m_used = m_new;
                 const float mc = m_new == -INFINITY ? 0.f : m_new * c;
-                // P tile g % PT is free once P V of block g - PT is done
-                if (g >= kPT && !warp_wait_parity(&o_done[(g - kPT) % kPT], ((g - kPT) / kPT) & 1, deadline,
-                                                  abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
                 // exp2, the row sum (four packed f32x2 accumulators), the rounding to the input type
-                // and the store to the swizzled P tile in one pass: half h of the row is 16-byte
-                // chunks 4 h .. 4 h + 3, and chunk j of row r sits at r * 128 + (j ^ (r % 8)) * 16
-                uint8_t* prow = sp + (g % kPT) * C::kPTile + lrow * 128;
+                // and the store of P in one pass: P of block g goes over the first 32 columns of its
+                // own S buffer (half h of the row: 16 columns of two values), whose scores are in
+                // registers by then; Q K^T refills the buffer only after P V of g has read it
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
                 auto exp_store = [&](int h, const float (&x)[32]) {
+                    uint32_t pv[16];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        uint32_t qv[4];
 #pragma unroll
                         for (int e = 0; e < 8; e += 2) {
                             const float2 y = fma2f(make_float2(x[8 * k + e], x[8 * k + e + 1]), make_float2(c, c),
                                                    make_float2(-mc, -mc));
                             const float2 ev = make_float2(ex2_approx(y.x), ex2_approx(y.y));
                             acc[e >> 1] = add2f(acc[e >> 1], ev);
-                            qv[e >> 1] = pack2<BF16>(ev.x, ev.y);
+                            pv[4 * k + (e >> 1)] = pack2<BF16>(ev.x, ev.y);
                         }
-                        const int chunk = (4 * h + k) ^ (lrow & 7);
-                        *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
                     }
+                    tmem_st_row16(tl + sb * 64 + 16 * h, pv);
                 };
                 exp_store(0, sc);
                 load_half(1, sc);
-                // this warp's lanes of S[sb] are no longer read: Q K^T of block g + 2 may reuse it
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[sb]);
                 exp_store(1, sc);
                 const float2 a2 = add2f(add2f(acc[0], acc[1]), add2f(acc[2], acc[3]));
                 l = l * alpha + (a2.x + a2.y);
@@ -676,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                     }
                     tmem_wait_st();
                 }
-                fence_proxy_async_smem();
+                tmem_wait_st();                         // P is in TMEM before P V reads it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[g % kPT]);
