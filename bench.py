@@ -426,20 +426,20 @@ def run_gpu(args):
     t_e0 = time.perf_counter()
     pipelined(3, hp, pin, prefill_step, pout, houts, dev)             # warm-up
     e_pre_ms = pipelined(e2e_steps, hp, pin, prefill_step, pout, houts, dev)
-    # the decode's copies are a few KB: a serial step (copies, kernel, copy back) beats the
-    # cross-stream events of the pipeline
-    e_dec_ms = 0.0
-    for i in range(e2e_steps + 2):
-        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the decode's copies are a few KB: its steps run one after another on one stream (copies in,
+    # kernel, copy back), all enqueued ahead so that no host gap falls inside a step's events
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(e2e_steps + 2)]
+    torch.cuda.synchronize()
+    for i, (a, c) in enumerate(dec_ev):
         a.record(stream)
         for d, h in zip(din[0], hdec):
             d.copy_(h, non_blocking=True)
         decode_step(0)
-        hdouts[0].copy_(dpout[0], non_blocking=True)
+        hdouts[i % 2].copy_(dpout[0], non_blocking=True)
         c.record(stream)
-        torch.cuda.synchronize()
-        if i >= 2:
-            e_dec_ms += a.elapsed_time(c)
+    torch.cuda.synchronize()
+    e_dec_ms = sum(a.elapsed_time(c) for a, c in dec_ev[2:])
     clocks.phase("e2e", t_e0, time.perf_counter())
     e_pre_s = max_over_ranks(e_pre_ms / 1e3, world, dev)
     e_dec_s = max_over_ranks(e_dec_ms / 1e3, world, dev)
