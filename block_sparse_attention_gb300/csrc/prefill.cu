@@ -30,6 +30,10 @@
 //               32w + t%16 of the M=64 accumulator, and read its two 32-column halves through
 //               the 16x32bx2 shape; three-input max, packed f32x2 FMA and adds) and the
 //               epilogue, which writes O / l from registers with 16-byte stores.
+// In the deeper d = 128 variant P stays in TMEM: the softmax writes it (16x32bx2 stores, in the
+// M = 64 accumulator layout) over the first 32 columns of its block's S buffer, P V reads it as
+// the A operand from tensor memory, and the commit of P V(g) frees S buffer g % 2 for Q K^T of
+// g + 2 -- no P tile to wait for and no shared-memory fence before P V.
 // Every mbarrier wait is polled by the whole warp (one non-blocking probe, then a bounded loop):
 // a wait by one lane behind a branch costs several times more on this hardware.
 // Rows that can span 1024+ key blocks and visit more than 96 are split into 64-block parts: the
@@ -184,6 +188,33 @@ __device__ __forceinline__ float2 add2f(float2 a, float2 b) {
     return d;
 }
 
+// 16 TMEM lanes x 32 bits in two halves, 16 columns each: lane t < 16 of the warp writes lane
+// (quarter base + t), columns [col, col + 16); lane t >= 16 writes lane (quarter base + t - 16),
+// columns [col + 16, col + 32).  For an M = 64 operand (rows 16w..16w+15 in lanes 32w..32w+15)
+// lanes t and t + 16 thus write the two 16-column halves of the same row.
+__device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16, issued by one lane of a converged warp under a guard
+// predicate; A in tensor memory in the accumulator layout of its M, two 16-bit values per column.
+__device__ __forceinline__ void mma_f16_ts_if(bool lead, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(lead ? 1u : 0u)
+        : "memory");
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (BF16) {
@@ -218,7 +249,7 @@ __device__ __forceinline__ void decode_item(int t, int BH, int nq, int win, int&
     bh = h0 + (r - (r / wh) * wh);
 }
 
-template <int D, bool BF16, bool DEEP, bool PAIR, bool SPLIT>
+template <int D, bool BF16, bool DEEP, bool PAIR, bool SPLIT, bool TPV = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -283,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(q_free, 1);
         for (int j = 0; j < kSB; ++j) {
             mbar_init(&s_full[j], 1);
-            mbar_init(&s_free[j], 4);                  // one arrival per softmax warp
+            // one arrival per softmax warp; with P in TMEM over S, the commit of P V of the block
+            mbar_init(&s_free[j], TPV ? 1 : 4);
         }
         for (int j = 0; j < kSlots; ++j) {
             mbar_init(&item_full[j], 1);
@@ -683,13 +715,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 tc_fence_after();
                 // descriptor start addresses advance by (byte offset >> 4): 16 keys of P are 32 bytes
                 // along its rows, 16 tokens of V are 16 rows of 128 bytes
-                const uint64_t a0 = p_desc + static_cast<uint32_t>(g % kPT) * (8192u >> 4);
                 const uint64_t b0 = v_desc + static_cast<uint32_t>(vs) * (kTile >> 4);
+                if constexpr (TPV) {
+                    // A = P of block g in TMEM over the first 32 columns of S buffer g % 2: 16 keys
+                    // are 8 columns
+                    const uint32_t a0 = tbase + 64 * (g & 1);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16_ss_if(lead, tbase + kOCol, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO,
-                                  (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16_ts_if(lead, tbase + kOCol, a0 + 8 * kk, b0 + ((kk * 2048) >> 4), idO,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                } else {
+                    const uint64_t a0 = p_desc + static_cast<uint32_t>(g % kPT) * (8192u >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16_ss_if(lead, tbase + kOCol, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit_if(lead, &o_done[g % kOD]);  // P V of g is done: O holds it, its P tile is free
+                if constexpr (TPV) mma_commit_if(lead, &s_free[g & 1]);   // S / P buffer g % 2 free
                 if constexpr (kVStages != 2) mma_commit_if(lead, &v_empty[vs]);   // V stage free
             }
             if (!ok) break;
@@ -880,10 +923,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 uint32_t r[32];
                 tmem_ld_16x32bx2_x32<32>(tl + sb * 64, r);
                 tmem_wait_ld();
-                // this warp's lanes of S[sb] are in registers: Q K^T of block g+2 may reuse it
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[sb]);
+                if constexpr (!TPV) {
+                    // this warp's lanes of S[sb] are in registers: Q K^T of block g+2 may reuse it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_free[sb]);
+                }
                 float s[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(r[e]);
@@ -936,9 +981,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 uint32_t pk[16];                  // P in the input type, ready for the P tile
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(s[2 * e], s[2 * e + 1]);
-                // P tile g % PT is free once P V of block g - PT is done
-                if (g >= kPT && !warp_wait_parity(&o_done[(g - kPT) % kOD], ((g - kPT) / kOD) & 1, deadline,
-                                                  abort_flag, status)) {
+                // P tile g % PT is free once P V of block g - PT is done (P in TMEM: it goes over
+                // this block's own S buffer, which Q K^T could only refill after that P V)
+                if (!TPV && g >= kPT && !warp_wait_parity(&o_done[(g - kPT) % kOD], ((g - kPT) / kOD) & 1, deadline,
+                                                          abort_flag, status)) {
                     ok = false;
                     break;
                 }
@@ -961,16 +1007,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                     tmem_wait_st();
                 }
-                // P -> the swizzled P tile: this lane's 32 columns are 16-byte chunks 4 hf .. 4 hf + 3
-                // of its row; a chunk c of row r sits at r * 128 + (c ^ (r % 8)) * 16
-                uint8_t* prow = sp + (g % kPT) * 8192 + lrow * 128;
+                if constexpr (TPV) {
+                    // P -> TMEM over the first 32 columns of S buffer sb (this lane's 32 keys are
+                    // 16 columns: the first or the second half of its row)
+                    tmem_st_16x32bx2_x16(tl + sb * 64, pk);
+                    tmem_wait_st();
+                } else {
+                    // P -> the swizzled P tile: this lane's 32 columns are 16-byte chunks
+                    // 4 hf .. 4 hf + 3 of its row; a chunk c of row r sits at r * 128 + (c ^ (r % 8)) * 16
+                    uint8_t* prow = sp + (g % kPT) * 8192 + lrow * 128;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int chunk = (4 * hf + k) ^ (lrow & 7);
-                    *reinterpret_cast<uint4*>(prow + chunk * 16) =
-                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int k = 0; k < 4; ++k) {
+                        const int chunk = (4 * hf + k) ^ (lrow & 7);
+                        *reinterpret_cast<uint4*>(prow + chunk * 16) =
+                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[g % kPF]);
@@ -1120,7 +1173,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-template <int D, bool BF16, bool DEEP, bool PAIR = false>
+template <int D, bool BF16, bool DEEP, bool PAIR = false, bool TPV = false>
 int launch(const void* q, const void* k, const void* v, const PrefillParams& prm,
            cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
@@ -1137,7 +1190,7 @@ int launch(const void* q, const void* k, const void* v, const PrefillParams& prm
     // rows are split across CTAs only when the continuation queue is set up (rows that can span
     // 1024+ key blocks): the kernel without that code is smaller, which keeps its hot loops in the
     // instruction cache
-    auto kern = prm.entries ? prefill_kernel<D, BF16, DEEP, PAIR, true> : prefill_kernel<D, BF16, DEEP, PAIR, false>;
+    auto kern = prm.entries ? prefill_kernel<D, BF16, DEEP, PAIR, true, TPV> : prefill_kernel<D, BF16, DEEP, PAIR, false, TPV>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSATTN_ERR_CUDA;
     int sms = num_sms_of_current_device();
@@ -1242,7 +1295,8 @@ extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
         return bf16 ? launch<64, true, false>(q, k, v, prm, st) : launch<64, false, false>(q, k, v, prm, st);
     }
     if (Layout<128, true>::bytes(nk) <= kSmemPerCtaMax)
-        return bf16 ? launch<128, true, true>(q, k, v, prm, st) : launch<128, false, true>(q, k, v, prm, st);
+        return bf16 ? launch<128, true, true, false, true>(q, k, v, prm, st)
+                    : launch<128, false, true, false, true>(q, k, v, prm, st);
     return bf16 ? launch<128, true, false>(q, k, v, prm, st) : launch<128, false, false>(q, k, v, prm, st);
 }
 
