@@ -30,10 +30,10 @@
 //               32w + t%16 of the M=64 accumulator, and read its two 32-column halves through
 //               the 16x32bx2 shape; three-input max, packed f32x2 FMA and adds) and the
 //               epilogue, which writes O / l from registers with 16-byte stores.
-// In the deeper d = 128 variant P stays in TMEM: the softmax writes it (16x32bx2 stores, in the
-// M = 64 accumulator layout) over the first 32 columns of its block's S buffer, P V reads it as
-// the A operand from tensor memory, and the commit of P V(g) frees S buffer g % 2 for Q K^T of
-// g + 2 -- no P tile to wait for and no shared-memory fence before P V.
+// In the deeper variants P stays in TMEM: the softmax writes it (16x32bx2 stores, in the M = 64
+// accumulator layout) over the first 32 columns of its block's S buffer, P V reads it as the A
+// operand from tensor memory, and the commit of P V(g) frees S buffer g % 2 for Q K^T of g + 2 --
+// no P tile to wait for and no shared-memory fence before P V.
 // Every mbarrier wait is polled by the whole warp (one non-blocking probe, then a bounded loop):
 // a wait by one lane behind a branch costs several times more on this hardware.
 // Rows that can span 1024+ key blocks and visit more than 96 are split into 64-block parts: the
@@ -75,31 +75,23 @@ constexpr int kSchedWarp = 7;           // fetches items, compacts their mask ro
 // the tiles are half the size, the rings deeper, and the stages have their own k_empty / v_empty
 // barriers.
 // The deeper variants are used whenever their shared memory (which grows with the mask-row lists)
-// fits: at d = 128 a third K stage in place of the second P tile (the K stream is on the critical
-// path there, and the softmax has slack to wait for P V of the previous block); at d = 64 four
-// K and four V stages.
-// The pair variant (d = 64, whenever its shared memory fits) hands key blocks to the softmax two
-// at a time: the softmax warps poll, fence and arrive once per pair instead of once per block,
-// and take one row maximum over both blocks.  It keeps three S buffers in TMEM (a pair's two, plus
-// one that the next pair's first Q K^T fills while the softmax works), four K and V stages, and
-// four P tiles (two pairs); p_full and o_done then count pairs.
+// fits: at d = 128 a third K stage in place of the second P tile, at d = 64 four K and four V
+// stages; both keep P in TMEM (the shared-memory P tiles then go unused).
 constexpr int kRingD64 = 4;
-template <int D, bool DEEP, bool PAIR = false>
+template <int D, bool DEEP>
 struct Rings {
-    static constexpr int kK = PAIR ? 4 : (D == 64 ? (DEEP ? kRingD64 : 2) : (DEEP ? 3 : 2));
-    static constexpr int kV = PAIR ? 4 : (D == 64 ? (DEEP ? kRingD64 : 2) : 2);
-    // P tiles: two (double-buffered), one in the deeper d = 128 variant, four in the pair variant.
-    // p_full and o_done have one barrier per P tile, at least two, so that at d = 128 o_done of
-    // block g also frees V stage g % 2 (two per pair of P tiles in the pair variant).  (Three P
-    // tiles at d = 64 measured 2 % slower than two on a 4x16x8192 fp16 prefill.)
-    static constexpr int kPTiles = PAIR ? 4 : ((D == 128 && DEEP) ? 1 : 2);
-    static constexpr int kPF = PAIR ? 2 : (kPTiles > 2 ? kPTiles : 2);
-    static constexpr int kOD = PAIR ? 2 : (kPTiles > 2 ? kPTiles : 2);
-    static constexpr int kSBuf = PAIR ? 3 : 2;       // S buffers in TMEM, 64 columns each
+    static constexpr int kK = D == 64 ? (DEEP ? kRingD64 : 2) : (DEEP ? 3 : 2);
+    static constexpr int kV = D == 64 ? (DEEP ? kRingD64 : 2) : 2;
+    // P tiles in shared memory: two (double-buffered), one in the deeper d = 128 variant.  p_full
+    // and o_done have one barrier per P tile, at least two, so that at d = 128 o_done of block g
+    // also frees V stage g % 2.  (Kernels that keep P in TMEM leave the P tiles unused.)
+    static constexpr int kPTiles = (D == 128 && DEEP) ? 1 : 2;
+    static constexpr int kPF = kPTiles > 2 ? kPTiles : 2;
+    static constexpr int kOD = kPTiles > 2 ? kPTiles : 2;
     static_assert(kV != 2 || kOD == 2, "two V stages are released through o_done[g % 2]");
-    static_assert(!PAIR || (D == 64 && kSBuf * 64 + D <= 256), "pair variant: S buffers and O in 256 columns");
 };
-constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d); pair: S[2] 128-191, O 192-255
+constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
+constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
 constexpr int kCtasPerSm = 2;
 constexpr int kSlots = 3;               // items published ahead of the consumers
@@ -140,20 +132,19 @@ struct PrefillParams {
     unsigned long long budget_ns;
 };
 
-template <int D, bool DEEP, bool PAIR = false>
+template <int D, bool DEEP>
 struct Layout {
-    using R = Rings<D, DEEP, PAIR>;
+    using R = Rings<D, DEEP>;
     static constexpr uint32_t kTile = (D / 64) * 8192;   // one [64 x D] 16-bit tile
     static constexpr uint32_t kQ = 0;                     // Q of the current item
     static constexpr uint32_t kK = kTile;
     static constexpr uint32_t kV = kK + R::kK * kTile;
     static constexpr uint32_t kP = kV + R::kV * kTile;   // [64 x 64] P tiles
     static constexpr uint32_t kBars = kP + R::kPTiles * 8192;
-    // q_full q_free k_full[KS] v_full[VS] s_full[SB] s_free[SB]
+    // q_full q_free k_full[KS] v_full[VS] s_full[2] s_free[2]
     // p_full[PF] o_done[OD] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
     // k_empty[KS] v_empty[VS]
-    static constexpr uint32_t kNumBars = 2 + 2 * (R::kK + R::kV) + 2 * R::kSBuf + R::kPF + R::kOD + 1 +
-                                         2 * kSlots + 5;
+    static constexpr uint32_t kNumBars = 2 + 2 * (R::kK + R::kV) + 4 + R::kPF + R::kOD + 1 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 28 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -249,12 +240,12 @@ __device__ __forceinline__ void decode_item(int t, int BH, int nq, int win, int&
     bh = h0 + (r - (r / wh) * wh);
 }
 
-template <int D, bool BF16, bool DEEP, bool PAIR, bool SPLIT, bool TPV = false>
+template <int D, bool BF16, bool DEEP, bool SPLIT, bool TPV>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = Layout<D, DEEP, PAIR>;
-    using R = Rings<D, DEEP, PAIR>;
+    using L = Layout<D, DEEP>;
+    using R = Rings<D, DEEP>;
     using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
     constexpr uint32_t kTile = L::kTile;
     constexpr int kKStages = R::kK;
@@ -262,8 +253,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     constexpr int kPT = R::kPTiles;
     constexpr int kPF = R::kPF;
     constexpr int kOD = R::kOD;
-    constexpr int kSB = R::kSBuf;
-    constexpr uint32_t kOCol = kSB * 64;              // O follows the S buffers in TMEM
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -276,10 +265,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* q_free = q_full + 1;
     uint64_t* k_full = q_free + 1;                 // [KS]
     uint64_t* v_full = k_full + kKStages;          // [VS]
-    uint64_t* s_full = v_full + kVStages;          // [SB] (at d = 128 it also frees K stage g % 2)
-    uint64_t* s_free = s_full + kSB;               // [SB]
-    uint64_t* p_full = s_free + kSB;               // [PF] P tile of block g written (index g % PF; pair variant: pair j, j % 2)
-    uint64_t* o_done = p_full + kPF;               // [OD] P V of block g done (index g % OD; pair variant: pair j, j % 2)
+    uint64_t* s_full = v_full + kVStages;          // [2] (at d = 128 it also frees K stage g % 2)
+    uint64_t* s_free = s_full + 2;                 // [2]
+    uint64_t* p_full = s_free + 2;                 // [PF] P of block g written (index g % PF)
+    uint64_t* o_done = p_full + kPF;               // [OD] P V of block g done (index g % OD)
     uint64_t* o_free = o_done + kOD;
     uint64_t* item_full = o_free + 1;              // [slots]
     uint64_t* item_empty = item_full + kSlots;     // [slots]
@@ -312,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (tid == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        for (int j = 0; j < kSB; ++j) {
+        for (int j = 0; j < 2; ++j) {
             mbar_init(&s_full[j], 1);
             // one arrival per softmax warp; with P in TMEM over S, the commit of P V of the block
             mbar_init(&s_free[j], TPV ? 1 : 4);
@@ -625,10 +614,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int i = 0; i < cnt; ++i) {
                     const int g = blk + i;
                     const int ks = g % kKStages;
-                    const int sb = kSB == 2 ? (g & 1) : g % kSB;
+                    const int sb = g & 1;
                     if (!warp_wait_parity(&k_full[ks], (g / kKStages) & 1, deadline, abort_flag, status) ||
-                        (g >= kSB && !warp_wait_parity(&s_free[sb], ((g / kSB) - 1) & 1, deadline, abort_flag,
-                                                       status))) {
+                        (g >= 2 && !warp_wait_parity(&s_free[sb], ((g - 2) >> 1) & 1, deadline, abort_flag,
+                                                     status))) {
                         ok = false;
                         break;
                     }
@@ -661,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         constexpr uint32_t idO = idesc_f16(64, D, BF16, true);
         const uint64_t p_desc = sdesc_sw128(smem_u32(sp), 16, 1024);
         const uint64_t v_desc = sdesc_sw128(smem_u32(sv), 8192, 1024);
-        int blk = 0, items = 0, pr = 0;
+        int blk = 0, items = 0;
         for (int n = 0;; ++n) {
             const int slot = n % kSlots;
             if (!warp_wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
@@ -669,37 +658,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int cnt = count_of[slot];
             if (item < 0) break;
             bool ok = true;
-            if constexpr (PAIR) {
-                // blocks two at a time: one p_full wait and one o_done commit per pair; pair pr
-                // reads P tiles 2 (pr % 2) and 2 (pr % 2) + 1
-                for (int i = 0; i < cnt; i += 2, ++pr) {
-                    const int n2 = cnt - i < 2 ? cnt - i : 2;
-                    if (!warp_wait_parity(&p_full[pr & 1], (pr >> 1) & 1, deadline, abort_flag, status) ||
-                        (i == 0 && items >= 1 &&
-                         !warp_wait_parity(o_free, (items - 1) & 1, deadline, abort_flag, status))) {
-                        ok = false;
-                        break;
-                    }
-                    for (int h = 0; h < n2; ++h) {
-                        const int g = blk + i + h;
-                        const int vs = g % kVStages;
-                        if (!warp_wait_parity(&v_full[vs], (g / kVStages) & 1, deadline, abort_flag, status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t a0 = p_desc + static_cast<uint32_t>(2 * (pr & 1) + h) * (8192u >> 4);
-                        const uint64_t b0 = v_desc + static_cast<uint32_t>(vs) * (kTile >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f16_ss_if(lead, tbase + kOCol, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4),
-                                          idO, (i + h > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit_if(lead, &v_empty[vs]);   // V stage free
-                    }
-                    if (!ok) break;
-                    mma_commit_if(lead, &o_done[pr & 1]);   // the pair's P V done: its P tiles are free
-                }
-            } else
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
                 const int vs = g % kVStages;
@@ -754,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int lrow = 16 * warp + (lane & 15);
         const uint32_t tl = tbase + (static_cast<uint32_t>(32 * warp) << 16);
         const float c = p.scale_log2;
-        int blk = 0, qloads = 0, nsplit = 0, pr = 0;
+        int blk = 0, qloads = 0, nsplit = 0;
         for (int n = 0;; ++n) {
             const int slot = n % kSlots;
             if (!warp_wait_parity(&item_full[slot], (n / kSlots) & 1, deadline, abort_flag, status)) break;
@@ -779,139 +737,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             float m_used = -INFINITY;
             float l = 0.f;
             bool ok = true;
-            if constexpr (PAIR) {
-                // key blocks two at a time (a pair's blocks belong to one item; an odd count ends
-                // with a single block): one row maximum over both, P of both into P tiles
-                // 2 (pr % 2) and 2 (pr % 2) + 1, one fence and one p_full arrival per pair.  The
-                // scores are read from TMEM in two passes so that one block's 32 scores at a time
-                // are live: the second block's only for its maximum, then the first block's (its S
-                // buffer is released at once, so the next pair's Q K^T can refill it), and the
-                // second block's again after the first one's P is stored.
-                for (int i = 0; i < cnt; i += 2, ++pr) {
-                    const int g0 = blk + i;
-                    const bool two = i + 1 < cnt;
-                    const int g1 = two ? g0 + 1 : g0;
-                    // the commit after the pair's last Q K^T also covers the first one
-                    if (!warp_wait_parity(&s_full[g1 % kSB], (g1 / kSB) & 1, deadline, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int key0 = static_cast<int>(list[i]) * 64 + 32 * hf;
-                    const int key1 = two ? static_cast<int>(list[i + 1]) * 64 + 32 * hf : key0;
-                    const bool edge0 = key0 + 31 >= p.Sk || (p.causal && key0 + 31 > row + past);
-                    const bool edge1 = key1 + 31 >= p.Sk || (p.causal && key1 + 31 > row + past);
-                    // scores of one block, masked on the diagonal / sequence tail
-                    auto load_scores = [&](int g, int key, bool edge, float (&sc)[32]) {
-                        uint32_t r[32];
-                        tmem_ld_16x32bx2_x32<32>(tl + (g % kSB) * 64, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) sc[e] = __uint_as_float(r[e]);
-                        if (edge) {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (key + e >= p.Sk || (p.causal && key + e > row + past)) sc[e] = -INFINITY;
-                        }
-                    };
-                    // maximum of 32 scores: four chains of three-input maxima
-                    auto max32 = [&](const float (&sc)[32]) -> float {
-                        float m4[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            float x = max3f(sc[j], sc[j + 4], sc[j + 8]);
-                            x = max3f(x, sc[j + 12], sc[j + 16]);
-                            x = max3f(x, sc[j + 20], sc[j + 24]);
-                            m4[j] = fmaxf(x, sc[j + 28]);
-                        }
-                        return fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
-                    };
-                    float sc[32];
-                    float m1 = -INFINITY;
-                    if (two) {
-                        load_scores(g1, key1, edge1, sc);
-                        m1 = max32(sc);
-                    }
-                    load_scores(g0, key0, edge0, sc);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_free[g0 % kSB]);   // block g0's S is in registers
-                    const float m0 = fmaxf(max32(sc), m1);
-                    const float mx = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 16));
-                    const bool grow = mx * c > m_used * c + kRescaleLog2;
-                    const float m_new = grow ? mx : m_used;
-                    const float alpha = grow ? ex2_approx((m_used - m_new) * c) : 1.f;
-                    const bool rescale_o = grow && m_used != -INFINITY;
-                    m_used = m_new;
-                    const float mc = m_new == -INFINITY ? 0.f : m_new * c;
-                    // the pair's P tiles are free once P V of pair pr - 2 is done (four tiles: by now
-                    // that is almost always so)
-                    if (pr >= 2 && !warp_wait_parity(&o_done[pr & 1], ((pr - 2) >> 1) & 1, deadline, abort_flag,
-                                                     status)) {
-                        ok = false;
-                        break;
-                    }
-                    // exp2, the row sum (four packed f32x2 accumulators), the rounding to the input type
-                    // and the store to the swizzled P tile in one pass; this lane's 32 columns of a
-                    // block are 16-byte chunks 4 hf .. 4 hf + 3 of its row, and chunk c of row r sits
-                    // at r * 128 + (c ^ (r % 8)) * 16
-                    uint8_t* prow = sp + (2 * (pr & 1)) * 8192 + lrow * 128;
-                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                     make_float2(0.f, 0.f)};
-                    auto exp_store = [&](const float (&x)[32], uint8_t* dst) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint32_t qv[4];
-#pragma unroll
-                            for (int e = 0; e < 8; e += 2) {
-                                const float2 y = fma2f(make_float2(x[8 * k + e], x[8 * k + e + 1]), make_float2(c, c),
-                                                       make_float2(-mc, -mc));
-                                const float2 ev = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-                                acc[e >> 1] = add2f(acc[e >> 1], ev);
-                                qv[e >> 1] = pack2<BF16>(ev.x, ev.y);
-                            }
-                            const int chunk = (4 * hf + k) ^ (lrow & 7);
-                            *reinterpret_cast<uint4*>(dst + chunk * 16) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
-                        }
-                    };
-                    exp_store(sc, prow);
-                    if (two) {
-                        load_scores(g1, key1, edge1, sc);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&s_free[g1 % kSB]);
-                        exp_store(sc, prow + 8192);
-                    }
-                    const float2 a2 = add2f(add2f(acc[0], acc[1]), add2f(acc[2], acc[3]));
-                    const float sum0 = a2.x + a2.y;
-                    const float sum = sum0 + __shfl_xor_sync(0xffffffffu, sum0, 16);
-                    l = l * alpha + sum;
-                    if (__any_sync(0xffffffffu, rescale_o)) {
-                        // O is scaled once it holds every pair before this one (before p_full lets
-                        // P V of this pair add to it)
-                        if (pr >= 1 && !warp_wait_parity(&o_done[(pr - 1) & 1], ((pr - 1) >> 1) & 1, deadline,
-                                                         abort_flag, status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll 1
-                        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                            uint32_t o[32];
-                            tmem_ld_16x32bx2_x32<D / 2>(tl + kOCol + c0, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st_16x32bx2_x32<D / 2>(tl + kOCol + c0, o);
-                        }
-                        tmem_wait_st();
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[pr & 1]);
-                }
-            } else
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
                 const int sb = g & 1;
@@ -1030,13 +855,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
             if (!ok) break;
             // ---- epilogue: O / l, written from registers straight to global memory
-            if constexpr (PAIR) {
-                if (!warp_wait_parity(&o_done[(pr - 1) & 1], ((pr - 1) >> 1) & 1, deadline, abort_flag, status))
-                    break;
-            } else {
-                const int glast = blk + cnt - 1;
-                if (!warp_wait_parity(&o_done[glast % kOD], (glast / kOD) & 1, deadline, abort_flag, status)) break;
-            }
+            const int glast = blk + cnt - 1;
+            if (!warp_wait_parity(&o_done[glast % kOD], (glast / kOD) & 1, deadline, abort_flag, status)) break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             if (SPLIT && nparts > 1) {
@@ -1173,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-template <int D, bool BF16, bool DEEP, bool PAIR = false, bool TPV = false>
+template <int D, bool BF16, bool DEEP, bool TPV = false>
 int launch(const void* q, const void* k, const void* v, const PrefillParams& prm,
            cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
@@ -1184,13 +1004,13 @@ int launch(const void* q, const void* k, const void* v, const PrefillParams& prm
     rc |= encode_3d(&tv, v, BF16, D, prm.Sk, BH, D * 2ull, uint64_t(prm.Sk) * D * 2, 64, 64, 1, true);
     if (rc) return rc;
     // at most two CTAs per SM: each holds 256 of the SM's 512 TMEM columns
-    uint32_t smem = Layout<D, DEEP, PAIR>::bytes(prm.nk);
+    uint32_t smem = Layout<D, DEEP>::bytes(prm.nk);
     if (smem < 78u * 1024u) smem = 78u * 1024u;
     if (smem > kSmemPerCtaMax) return BSATTN_ERR_UNSUPPORTED;
     // rows are split across CTAs only when the continuation queue is set up (rows that can span
     // 1024+ key blocks): the kernel without that code is smaller, which keeps its hot loops in the
     // instruction cache
-    auto kern = prm.entries ? prefill_kernel<D, BF16, DEEP, PAIR, true, TPV> : prefill_kernel<D, BF16, DEEP, PAIR, false, TPV>;
+    auto kern = prm.entries ? prefill_kernel<D, BF16, DEEP, true, TPV> : prefill_kernel<D, BF16, DEEP, false, TPV>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSATTN_ERR_CUDA;
     int sms = num_sms_of_current_device();
@@ -1280,23 +1100,17 @@ extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.budget_ns = wait_budget_ns();
     const bool bf16 = dtype == BSATTN_BF16;
-    // the deeper rings whenever they fit beside the mask-row lists (up to 4024 key blocks at
-    // d = 64, 1304 at d = 128), else two stages (up to 2672 key blocks at d = 128)
+    // the deeper rings, with P in TMEM, whenever they fit beside the mask-row lists (up to 4024
+    // key blocks at d = 64, 1304 at d = 128), else two stages (up to 2672 key blocks at d = 128)
     if (d == 64) {
-        // pairs of key blocks per softmax step when every CTA has work: a launch with fewer items
-        // than CTAs is bound by the latency of single items, which pairs lengthen
-        int sms = num_sms_of_current_device();
-        if (sms <= 0) sms = 148;
-        if (prm.total_items >= kCtasPerSm * sms && Layout<64, true, true>::bytes(nk) <= kSmemPerCtaMax)
+        if (Layout<64, true>::bytes(nk) <= kSmemPerCtaMax)
             return bf16 ? launch<64, true, true, true>(q, k, v, prm, st)
                         : launch<64, false, true, true>(q, k, v, prm, st);
-        if (Layout<64, true>::bytes(nk) <= kSmemPerCtaMax)
-            return bf16 ? launch<64, true, true>(q, k, v, prm, st) : launch<64, false, true>(q, k, v, prm, st);
         return bf16 ? launch<64, true, false>(q, k, v, prm, st) : launch<64, false, false>(q, k, v, prm, st);
     }
     if (Layout<128, true>::bytes(nk) <= kSmemPerCtaMax)
-        return bf16 ? launch<128, true, true, false, true>(q, k, v, prm, st)
-                    : launch<128, false, true, false, true>(q, k, v, prm, st);
+        return bf16 ? launch<128, true, true, true>(q, k, v, prm, st)
+                    : launch<128, false, true, true>(q, k, v, prm, st);
     return bf16 ? launch<128, true, false>(q, k, v, prm, st) : launch<128, false, false>(q, k, v, prm, st);
 }
 
