@@ -83,15 +83,17 @@ struct Rings {
     static constexpr int kK = D == 64 ? (DEEP ? kRingD64 : 2) : (DEEP ? 3 : 2);
     static constexpr int kV = D == 64 ? (DEEP ? kRingD64 : 2) : 2;
     // P tiles in shared memory: two (double-buffered), one in the deeper d = 128 variant.  p_full
-    // and o_done have one barrier per P tile, at least two, so that at d = 128 o_done of block g
-    // also frees V stage g % 2.  (Kernels that keep P in TMEM leave the P tiles unused.)
+    // and o_done are rings of parity barriers indexed by block: two at d = 128, where o_done of
+    // block g also frees V stage g % 2; four in the deeper d = 64 variant, whose three S buffers
+    // let the softmax run three blocks ahead of P V (a ring of two would then let a parity wait
+    // on block g pass on the phase of block g - 2).  (Kernels that keep P in TMEM leave the P
+    // tiles unused.)
     static constexpr int kPTiles = (D == 128 && DEEP) ? 1 : 2;
-    static constexpr int kPF = kPTiles > 2 ? kPTiles : 2;
-    static constexpr int kOD = kPTiles > 2 ? kPTiles : 2;
+    static constexpr int kPF = (D == 64 && DEEP) ? 4 : 2;
+    static constexpr int kOD = (D == 64 && DEEP) ? 4 : 2;
     static_assert(kV != 2 || kOD == 2, "two V stages are released through o_done[g % 2]");
 };
-constexpr uint32_t kTmemCols = 256;     // S[0] cols 0-63, S[1] 64-127, O 128-(128+d)
-constexpr uint32_t kOCol = 128;
+constexpr uint32_t kTmemCols = 256;     // S buffers of 64 columns from 0, then O (d columns)
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
 constexpr int kCtasPerSm = 2;
 constexpr int kSlots = 3;               // items published ahead of the consumers
@@ -144,7 +146,7 @@ struct Layout {
     // q_full q_free k_full[KS] v_full[VS] s_full[2] s_free[2]
     // p_full[PF] o_done[OD] o_free item_full[slots] item_empty[slots] fin_s fin_pv loaded pdone mdec
     // k_empty[KS] v_empty[VS]
-    static constexpr uint32_t kNumBars = 2 + 2 * (R::kK + R::kV) + 4 + R::kPF + R::kOD + 1 + 2 * kSlots + 5;
+    static constexpr uint32_t kNumBars = 2 + 2 * (R::kK + R::kV) + 6 + R::kPF + R::kOD + 1 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 28 * kSlots + 16;
     __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
@@ -253,6 +255,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     constexpr int kPT = R::kPTiles;
     constexpr int kPF = R::kPF;
     constexpr int kOD = R::kOD;
+    // S buffers in TMEM (64 columns each): three at d = 64 with P in TMEM (P over its S buffer ties
+    // the buffer up until P V is done, and 3 x 64 + 64 columns fit), else two; O follows them
+    constexpr int kSB = (TPV && D == 64) ? 3 : 2;
+    constexpr uint32_t kOCol = kSB * 64;
+    static_assert(kPF >= kSB && kOD >= kSB, "p_full / o_done rings at least as deep as the S buffers");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -265,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint64_t* q_free = q_full + 1;
     uint64_t* k_full = q_free + 1;                 // [KS]
     uint64_t* v_full = k_full + kKStages;          // [VS]
-    uint64_t* s_full = v_full + kVStages;          // [2] (at d = 128 it also frees K stage g % 2)
-    uint64_t* s_free = s_full + 2;                 // [2]
-    uint64_t* p_full = s_free + 2;                 // [PF] P of block g written (index g % PF)
+    uint64_t* s_full = v_full + kVStages;          // [SB] (at d = 128 without TMEM P it also frees K stage g % 2)
+    uint64_t* s_free = s_full + 3;                 // [SB]
+    uint64_t* p_full = s_free + 3;                 // [PF] P of block g written (index g % PF)
     uint64_t* o_done = p_full + kPF;               // [OD] P V of block g done (index g % OD)
     uint64_t* o_free = o_done + kOD;
     uint64_t* item_full = o_free + 1;              // [slots]
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (tid == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kSB; ++j) {
             mbar_init(&s_full[j], 1);
             // one arrival per softmax warp; with P in TMEM over S, the commit of P V of the block
             mbar_init(&s_free[j], TPV ? 1 : 4);
@@ -614,10 +621,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int i = 0; i < cnt; ++i) {
                     const int g = blk + i;
                     const int ks = g % kKStages;
-                    const int sb = g & 1;
+                    const int sb = kSB == 2 ? (g & 1) : g % kSB;
                     if (!warp_wait_parity(&k_full[ks], (g / kKStages) & 1, deadline, abort_flag, status) ||
-                        (g >= 2 && !warp_wait_parity(&s_free[sb], ((g - 2) >> 1) & 1, deadline, abort_flag,
-                                                     status))) {
+                        (g >= kSB && !warp_wait_parity(&s_free[sb], ((g / kSB) - 1) & 1, deadline, abort_flag,
+                                                       status))) {
                         ok = false;
                         break;
                     }
@@ -677,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if constexpr (TPV) {
                     // A = P of block g in TMEM over the first 32 columns of S buffer g % 2: 16 keys
                     // are 8 columns
-                    const uint32_t a0 = tbase + 64 * (g & 1);
+                    const uint32_t a0 = tbase + 64 * (kSB == 2 ? (g & 1) : g % kSB);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_f16_ts_if(lead, tbase + kOCol, a0 + 8 * kk, b0 + ((kk * 2048) >> 4), idO,
@@ -690,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                       (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit_if(lead, &o_done[g % kOD]);  // P V of g is done: O holds it, its P tile is free
-                if constexpr (TPV) mma_commit_if(lead, &s_free[g & 1]);   // S / P buffer g % 2 free
+                if constexpr (TPV) mma_commit_if(lead, &s_free[kSB == 2 ? (g & 1) : g % kSB]);   // S / P buffer free
                 if constexpr (kVStages != 2) mma_commit_if(lead, &v_empty[vs]);   // V stage free
             }
             if (!ok) break;
@@ -739,8 +746,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             bool ok = true;
             for (int i = 0; i < cnt; ++i) {
                 const int g = blk + i;
-                const int sb = g & 1;
-                if (!warp_wait_parity(&s_full[sb], (g >> 1) & 1, deadline, abort_flag, status)) {
+                const int sb = kSB == 2 ? (g & 1) : g % kSB;
+                if (!warp_wait_parity(&s_full[sb], (g / kSB) & 1, deadline, abort_flag, status)) {
                     ok = false;
                     break;
                 }
