@@ -14,12 +14,14 @@
 // Persistent kernel: two CTAs per SM (each holds half of the SM's 512 TMEM columns) pull work
 // items from an atomic counter in the workspace.  Items are ordered from the last query block
 // to the first across all heads (under a causal mask the late blocks visit the most keys), so
-// the longest items start first and the tail is short.  Warp roles (256 threads):
+// the longest items start first and the tail is short.  Warp roles (288 threads):
 //   warp 7      scheduler: claims the next item from the counter one ahead (not while the CTA
-//               is on a long row) and pulls its mask row into L2; publishes it once the producer
-//               has issued the previous item's K loads, after compacting its mask row;
-//   warp 5      producers: lane 0 loads each item's Q and streams its K tiles, lane 1 streams
-//               its V tiles, into K and V rings -- running ahead across items.  Two stages
+//               is on a long row) and pulls its mask row and its Q tile into L2; publishes it
+//               once the producer has issued the previous item's K loads, after compacting its
+//               mask row;
+//   warps 5, 8  producers: warp 5 loads each item's Q and streams its K tiles, warp 8 streams
+//               its V tiles, into K and V rings -- running ahead across items (one lane each: in
+//               separate warps neither stream's waits hold up the other's issue).  Two stages
 //               each at d = 128 (three K stages and one P tile in the deeper variant, used
 //               whenever its shared memory fits), four each at d = 64;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
@@ -63,11 +65,12 @@
 namespace bsattn {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr int kSWarp = 4;               // issues Q K^T, owns TMEM
 constexpr int kProdWarp = 5;            // TMA producer
 constexpr int kPVWarp = 6;              // issues P V
 constexpr int kSchedWarp = 7;           // fetches items, compacts their mask rows
+constexpr int kVProdWarp = 8;           // TMA producer of the V tiles
 // K and V rings: a K stage frees when the Q K^T reading it is done, a V stage when its P V is
 // done.  At d = 128 two stages of each are what shared memory allows beside Q and P at two CTAs
 // per SM; then K stage g % 2 and S buffer g & 1 of block g coincide, so the commit that completes
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         for (int j = 0; j < kSlots; ++j) {
             mbar_init(&item_full[j], 1);
-            mbar_init(&item_empty[j], 4 + 4);          // 2 producer lanes, S and PV issuers, 4 softmax warps
+            mbar_init(&item_empty[j], 4 + 4);          // 2 producers, S and PV issuers, 4 softmax warps
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -354,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const long long head_kv = 4LL * p.Sk * D;
         const long long wq = (32LL << 20) / (head_kv > 0 ? head_kv : 1);
         const int win = static_cast<int>(wq < 1 ? 1 : (wq > BH ? BH : wq));
-        // the next fresh item is claimed one ahead, and its mask row pulled into L2, so that
-        // neither the counter's round trip nor the row's first read delays publishing it
+        // the next fresh item is claimed one ahead, and its mask row and Q tile pulled into L2,
+        // so that neither the counter's round trip nor the row's first read delays publishing
+        // it, and its Q load (issued once the previous item's Q K^T is done) hits L2
         auto fresh = [&]() -> int {
             int v = 0;
             if (lane == 0) v = atomicAdd(p.ws + kWsNext, 1);
@@ -366,6 +370,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint8_t* row = p.mask + (static_cast<size_t>(pbh) * p.mq + (pqb >> p.bshift)) * p.mk;
                 for (int off = lane * 128; off < p.mk; off += 32 * 128)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+                if (lane == 0)
+                    for (int h = 0; h < D / 64; ++h)
+                        asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                                         reinterpret_cast<uint64_t>(&tm_q)),
+                                     "r"(h * 64), "r"(pqb * 64), "r"(pbh)
+                                     : "memory");
             }
             return v;
         };
@@ -518,13 +528,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (took_fresh && (e >= 0 || count <= p.long_row)) next_t = fresh();
             else if (took_fresh) next_t = -1;
         }
-    } else if (warp == kProdWarp) {
+    } else if (warp == kProdWarp || warp == kVProdWarp) {
         // ------------------------------------------------------------ TMA producers
-        // lane 0 streams each item's Q and K tiles, lane 1 its V tiles: the two rings drain
-        // at different points (a K stage after Q K^T, a V stage after P V), so neither stream
-        // waits for the other's slower ring
-        if (lane < 2) {
-            const bool kside = lane == 0;
+        // lane 0 of warp 5 streams each item's Q and K tiles, lane 0 of warp 8 its V tiles: the
+        // two rings drain at different points (a K stage after Q K^T, a V stage after P V), so
+        // neither stream waits for the other's slower ring
+        if (lane == 0) {
+            const bool kside = warp == kProdWarp;
             if (kside) {
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_k);
