@@ -23,7 +23,7 @@
 //               its V tiles, into K and V rings -- running ahead across items (one lane each: in
 //               separate warps neither stream's waits hold up the other's issue).  Two stages
 //               each at d = 128 (three K stages and one P tile in the deeper variant, used
-//               whenever its shared memory fits), four each at d = 64;
+//               whenever its shared memory fits), three each at d = 64;
 //   warp 4      allocates TMEM and issues Q K^T as soon as a K tile and an S buffer are free;
 //   warp 6      issues P V as soon as the softmax has written P (two issuing threads keep the
 //               M=64 tensor pipe fed: one thread issues at most about one MMA per 67 cycles);
@@ -72,25 +72,26 @@ constexpr int kPVWarp = 6;              // issues P V
 constexpr int kSchedWarp = 7;           // fetches items, compacts their mask rows
 constexpr int kVProdWarp = 8;           // TMA producer of the V tiles
 // K and V rings: a K stage frees when the Q K^T reading it is done, a V stage when its P V is
-// done.  At d = 128 two stages of each are what shared memory allows beside Q and P at two CTAs
-// per SM; then K stage g % 2 and S buffer g & 1 of block g coincide, so the commit that completes
-// S[g & 1] also frees the K stage (and o_done frees V stage g % 2 with P tile g & 1).  At d = 64
-// the tiles are half the size, the rings deeper, and the stages have their own k_empty / v_empty
-// barriers.
-// The deeper variants are used whenever their shared memory (which grows with the mask-row lists)
-// fits: at d = 128 a third K stage in place of the second P tile, at d = 64 four K and four V
-// stages; both keep P in TMEM (the shared-memory P tiles then go unused).
-constexpr int kRingD64 = 4;
+// done.  Where a ring is as deep as the S buffers, its stage g % SB coincides with S buffer g % SB
+// of block g, and the commits that complete S (Q K^T) or free the S buffer (P V) also free the
+// stage: fewer tcgen05.commit per block, each of which occupies the tensor core's issue pipe.
+// At d = 128 two stages of each are what shared memory allows beside Q and P at two CTAs per SM;
+// the deeper d = 128 variant has a third K stage with its own k_empty barrier.  At d = 64 the
+// deeper variant has three K and three V stages, as deep as its three S buffers (four stages
+// with their own release barriers measured 3 % slower on the C4 workload).  The deeper variants
+// keep P in TMEM (the shared-memory P tiles then go unused) and are used whenever their shared
+// memory (which grows with the mask-row lists) fits: always at d = 64, up to 1304 key blocks at
+// d = 128.
+constexpr int kRingD64 = 3;
 template <int D, bool DEEP>
 struct Rings {
     static constexpr int kK = D == 64 ? (DEEP ? kRingD64 : 2) : (DEEP ? 3 : 2);
     static constexpr int kV = D == 64 ? (DEEP ? kRingD64 : 2) : 2;
     // P tiles in shared memory: two (double-buffered), one in the deeper d = 128 variant.  p_full
-    // and o_done are rings of parity barriers indexed by block: two at d = 128, where o_done of
-    // block g also frees V stage g % 2; four in the deeper d = 64 variant, whose three S buffers
-    // let the softmax run three blocks ahead of P V (a ring of two would then let a parity wait
-    // on block g pass on the phase of block g - 2).  (Kernels that keep P in TMEM leave the P
-    // tiles unused.)
+    // and o_done are rings of parity barriers indexed by block: two at d = 128; four in the deeper
+    // d = 64 variant, whose three S buffers let the softmax run three blocks ahead of P V (a ring
+    // of two would then let a parity wait on block g pass on the phase of block g - 2).  Kernels
+    // that keep P in TMEM use neither the P tiles nor o_done (s_free marks P V done).
     static constexpr int kPTiles = (D == 128 && DEEP) ? 1 : 2;
     static constexpr int kPF = (D == 64 && DEEP) ? 4 : 2;
     static constexpr int kOD = (D == 64 && DEEP) ? 4 : 2;
@@ -152,8 +153,8 @@ struct Layout {
     static constexpr uint32_t kNumBars = 2 + 2 * (R::kK + R::kV) + 6 + R::kPF + R::kOD + 1 + 2 * kSlots + 5;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, per-slot item info
     static constexpr uint32_t kList = kMisc + 16 + 28 * kSlots + 16;
-    __host__ __device__ static uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
-    static uint32_t bytes(int nk) { return 1024 + kList + kSlots * list_stride(nk); }
+    __host__ __device__ static constexpr uint32_t list_stride(int nk) { return (2 * nk + 15) & ~15; }
+    static constexpr uint32_t bytes(int nk) { return 1024 + kList + kSlots * list_stride(nk); }
 };
 
 // max(a, b, c) in one instruction (three-input max.f32)
@@ -262,6 +263,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // the buffer up until P V is done, and 3 x 64 + 64 columns fit), else two; O follows them
     constexpr int kSB = (TPV && D == 64) ? 3 : 2;
     constexpr uint32_t kOCol = kSB * 64;
+    // Barriers that do double duty keep the tcgen05.commit count per block down (each commit
+    // occupies the tensor core's issue pipe, which limits the d = 64 kernels): with P in TMEM the
+    // commit that frees an S buffer after P V also marks that P V done (the epilogue and the O
+    // rescale wait on it) and frees V stage g % SB when the V ring is as deep as the S buffers;
+    // the commit that completes S frees K stage g % SB when the K ring is.  Without P in TMEM,
+    // o_done marks P V done and frees V stage g % 2.
+    constexpr bool kKbyS = kKStages == kSB;
+    constexpr bool kVbyS = TPV && kVStages == kSB;
+    constexpr bool kVbyO = !TPV && kVStages == 2;
     static_assert(kPF >= kSB && kOD >= kSB, "p_full / o_done rings at least as deep as the S buffers");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -564,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int ks = kblk % kKStages;
                             if (kblk >= kKStages &&
-                                !wait_parity(kKStages == 2 ? &s_full[ks] : &k_empty[ks], ((kblk / kKStages) - 1) & 1,
+                                !wait_parity(kKbyS ? &s_full[ks] : &k_empty[ks], ((kblk / kKStages) - 1) & 1,
                                              deadline, abort_flag,
                                              status)) {
                                 ok = false;
@@ -579,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int vs = vblk % kVStages;
                             if (vblk >= kVStages &&
-                                !wait_parity(kVStages == 2 ? &o_done[vs] : &v_empty[vs], ((vblk / kVStages) - 1) & 1,
+                                !wait_parity(kVbyS ? &s_free[vs] : (kVbyO ? &o_done[vs] : &v_empty[vs]), ((vblk / kVStages) - 1) & 1,
                                              deadline, abort_flag,
                                              status)) {
                                 ok = false;
@@ -648,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                       kk > 0 ? 1u : 0u);
                     }
                     mma_commit_if(lead, &s_full[sb]);
-                    if constexpr (kKStages != 2) mma_commit_if(lead, &k_empty[ks]);   // K stage free
+                    if constexpr (!kKbyS) mma_commit_if(lead, &k_empty[ks]);   // K stage free
                     if (i == cnt - 1) mma_commit_if(lead, q_free);   // Q no longer read
                 }
                 blk += cnt;
@@ -706,9 +716,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         mma_f16_ss_if(lead, tbase + kOCol, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO,
                                       (i > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit_if(lead, &o_done[g % kOD]);  // P V of g is done: O holds it, its P tile is free
+                if constexpr (!TPV) mma_commit_if(lead, &o_done[g % kOD]);  // P V of g done: its P tile is free
                 if constexpr (TPV) mma_commit_if(lead, &s_free[kSB == 2 ? (g & 1) : g % kSB]);   // S / P buffer free
-                if constexpr (kVStages != 2) mma_commit_if(lead, &v_empty[vs]);   // V stage free
+                if constexpr (!kVbyS && !kVbyO) mma_commit_if(lead, &v_empty[vs]);   // V stage free
             }
             if (!ok) break;
             if (cnt > 0) {
@@ -832,7 +842,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 if (__any_sync(0xffffffffu, rescale_o)) {
                     // O is scaled once it holds every block before g: P V of g-1 must be done
-                    if (g >= 1 && !warp_wait_parity(&o_done[(g - 1) % kOD], ((g - 1) / kOD) & 1, deadline,
+                    if (g >= 1 && !warp_wait_parity(TPV ? &s_free[(g - 1) % kSB] : &o_done[(g - 1) % kOD],
+                                                    TPV ? ((g - 1) / kSB) & 1 : ((g - 1) / kOD) & 1, deadline,
                                                     abort_flag, status)) {
                         ok = false;
                         break;
@@ -873,7 +884,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (!ok) break;
             // ---- epilogue: O / l, written from registers straight to global memory
             const int glast = blk + cnt - 1;
-            if (!warp_wait_parity(&o_done[glast % kOD], (glast / kOD) & 1, deadline, abort_flag, status)) break;
+            if (!warp_wait_parity(TPV ? &s_free[glast % kSB] : &o_done[glast % kOD],
+                                  TPV ? (glast / kSB) & 1 : (glast / kOD) & 1, deadline, abort_flag, status))
+                break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             if (SPLIT && nparts > 1) {
@@ -1117,14 +1130,12 @@ extern "C" int bsattn_prefill_bs(const void* q, const void* k, const void* v,
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.budget_ns = wait_budget_ns();
     const bool bf16 = dtype == BSATTN_BF16;
-    // the deeper rings, with P in TMEM, whenever they fit beside the mask-row lists (up to 4024
-    // key blocks at d = 64, 1304 at d = 128), else two stages (up to 2672 key blocks at d = 128)
-    if (d == 64) {
-        if (Layout<64, true>::bytes(nk) <= kSmemPerCtaMax)
-            return bf16 ? launch<64, true, true, true>(q, k, v, prm, st)
-                        : launch<64, false, true, true>(q, k, v, prm, st);
-        return bf16 ? launch<64, true, false>(q, k, v, prm, st) : launch<64, false, false>(q, k, v, prm, st);
-    }
+    // the deeper rings, with P in TMEM, whenever they fit beside the mask-row lists (every width
+    // up to 4096 key blocks at d = 64, up to 1304 at d = 128), else two stages (up to 2672 key
+    // blocks at d = 128)
+    static_assert(Layout<64, true>::bytes(4096) <= kSmemPerCtaMax, "d = 64 always runs the deeper rings");
+    if (d == 64)
+        return bf16 ? launch<64, true, true, true>(q, k, v, prm, st) : launch<64, false, true, true>(q, k, v, prm, st);
     if (Layout<128, true>::bytes(nk) <= kSmemPerCtaMax)
         return bf16 ? launch<128, true, true, true>(q, k, v, prm, st)
                     : launch<128, false, true, true>(q, k, v, prm, st);

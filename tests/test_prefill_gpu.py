@@ -257,10 +257,11 @@ def test_long_rows_split_across_ctas(bsa):
 
 
 @pytest.mark.parametrize("S,d", [(96000, 128), (258000, 64)])
-def test_wide_masks_run_the_two_stage_kernels(bsa, S, d):
-    """Masks too wide for the deeper rings' shared memory (more than 1304 key blocks at d = 128,
-    more than 4024 at d = 64) run the kernels with two-stage K/V rings: sampled rows match the
-    oracle."""
+def test_wide_masks(bsa, S, d):
+    """The widest masks: at d = 128 more than 1304 key blocks, too wide for the deeper rings'
+    shared memory, run the kernel with two-stage K/V rings; at d = 64 the deeper rings take every
+    width the library accepts (here 4032 key blocks, rows split across CTAs).  Sampled rows match
+    the oracle."""
     dev = torch.device("cuda")
     dtype = torch.bfloat16 if d == 128 else torch.float16
     q, k, v = synthetic.qkv(1, 1, S, S, d, dtype, seed=23)
