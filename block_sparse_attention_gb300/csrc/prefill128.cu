@@ -78,8 +78,8 @@ struct Cfg {
     static constexpr uint32_t kV = kK + kKS * kKTile;
     static constexpr uint32_t kBars = kV + kVS * kKTile;
     // q_full q_free k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] s_free[2]
-    // p_full[PT] o_done[PT] o_free item_full[slots] item_empty[slots] loaded fin_s fin_pv
-    static constexpr uint32_t kNumBars = 2 + 2 * kKS + 2 * kVS + 4 + 2 * kPT + 1 + 2 * kSlots + 3;
+    // p_full[PT] o_free item_full[slots] item_empty[slots] loaded fin_s fin_pv
+    static constexpr uint32_t kNumBars = 2 + 2 * kKS + 2 * kVS + 4 + kPT + 1 + 2 * kSlots + 3;
     static constexpr uint32_t kMisc = kBars + 8 * kNumBars;   // tmem, abort, then 4 ints per slot
     static constexpr uint32_t kList = kMisc + 16 + 16 * kSlots;
     static constexpr uint32_t kSmemMax = kCtasPerSm == 2 ? 113u * 1024u : 227u * 1024u;
@@ -258,8 +258,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
     uint64_t* s_full = v_empty + kVS;     // [2] (one used when narrow)
     uint64_t* s_free = s_full + 2;        // [2]
     uint64_t* p_full = s_free + 2;        // [PT]
-    uint64_t* o_done = p_full + kPT;      // [PT] P V of block g done (index g % PT)
-    uint64_t* o_free = o_done + kPT;
+    uint64_t* o_free = p_full + kPT;
     uint64_t* item_full = o_free + 1;     // [slots]
     uint64_t* item_empty = item_full + kSlots;
     uint64_t* loaded = item_empty + kSlots;
@@ -297,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
         }
         for (int j = 0; j < kPT; ++j) {
             mbar_init(&p_full[j], 4);
-            mbar_init(&o_done[j], 1);
         }
         mbar_init(o_free, 4);
         for (int j = 0; j < kSlots; ++j) {
@@ -442,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                         for (int j = 0; ok && j < count; ++j) {
                             const int vs = vblk % kVS;
                             if (vblk >= kVS &&
-                                !wait_parity(&v_empty[vs], ((vblk / kVS) - 1) & 1, deadline, abort_flag, status)) {
+                                !wait_parity(kVS == 2 ? &s_free[vs] : &v_empty[vs], ((vblk / kVS) - 1) & 1, deadline,
+                                             abort_flag, status)) {
                                 ok = false;
                                 break;
                             }
@@ -557,9 +556,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                 for (int kk = 0; kk < 4; ++kk)
                     mma_f16_ts_if(lead, tbase + kOCol, a0 + 8 * kk, b0 + ((kk * 2048) >> 4), idO,
                                   (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_if(lead, &o_done[g % kPT]);   // P V of g done: O holds it
-                mma_commit_if(lead, &s_free[g & 1]);     // S / P buffer g % 2 free for Q K^T of g + 2
-                mma_commit_if(lead, &v_empty[vs]);       // V stage free
+                // P V of g done: S / P buffer g % 2 is free for Q K^T of g + 2, O holds block g (the
+                // epilogue and the O rescale wait on this commit too) and, with two V stages, V stage
+                // g % 2 is free; a deeper V ring has its own release barrier.  Fewer commits per tile
+                // leave more of the tensor core's issue pipe to the MMAs.
+                mma_commit_if(lead, &s_free[g & 1]);
+                if constexpr (kVS != 2) mma_commit_if(lead, &v_empty[vs]);
             }
             if (!ok) break;
             if (cnt > 0) {
@@ -677,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
                 l = l * alpha + (a2.x + a2.y);
                 if (__any_sync(0xffffffffu, rescale_o)) {
                     // O is scaled once it holds every block before g: P V of g - 1 must be done
-                    if (g >= 1 && !warp_wait_parity(&o_done[(g - 1) % kPT], ((g - 1) / kPT) & 1, deadline,
+                    if (g >= 1 && !warp_wait_parity(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1, deadline,
                                                     abort_flag, status)) {
                         ok = false;
                         break;
@@ -702,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, NARROW>::kCtasPerSm)
             if (!ok) break;
             // ---- epilogue: O / l, written from registers straight to global memory
             const int glast = blk + cnt - 1;
-            if (!warp_wait_parity(&o_done[glast % kPT], (glast / kPT) & 1, deadline, abort_flag, status)) break;
+            if (!warp_wait_parity(&s_free[glast & 1], (glast >> 1) & 1, deadline, abort_flag, status)) break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (static_cast<size_t>(bh) * p.Sq + row) * D);
