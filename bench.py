@@ -29,6 +29,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import sys
 import threading
@@ -74,10 +75,26 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
+def source_digest(paths) -> str:
+    """Hash of the code in the given source files, comments, indentation and blank lines left
+    out: a record taken on a kernel stays valid through comment edits, not through code edits."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for line in src.splitlines():
+            line = line.strip()
+            if line:
+                h.update(line.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    kernel source and on this workload: the hash covers the kernel's .cu file and the inline
-    helpers it includes (else None)."""
+    kernel code and on this workload: the hash covers the code of the kernel's .cu file and of
+    the inline helpers it includes (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -87,14 +104,11 @@ def traffic_record(kernel: str, workload: str):
     if not rec or rec.get("config") != workload:
         return None
     names = rec["source"] if isinstance(rec["source"], list) else [rec["source"]]
-    h = hashlib.sha256()
     try:
-        for name in names:
-            with open(os.path.join(ROOT, "block_sparse_attention_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
+        digest = source_digest([os.path.join(ROOT, "block_sparse_attention_gb300", "csrc", name)
+                                for name in names])
     except OSError:
         return None
-    digest = h.hexdigest()[:16]
     return rec["bytes_per_launch"] if digest == rec.get("source_sha256_16") else None
 
 

@@ -34,7 +34,8 @@
 //               epilogue, which writes O / l from registers with 16-byte stores.
 // In the deeper variants P stays in TMEM: the softmax writes it (16x32bx2 stores, in the M = 64
 // accumulator layout) over the first 32 columns of its block's S buffer, P V reads it as the A
-// operand from tensor memory, and the commit of P V(g) frees S buffer g % 2 for Q K^T of g + 2 --
+// operand from tensor memory, and the commit of P V(g) frees that S buffer for the Q K^T of the
+// block that reuses it (g + 2; g + 3 at d = 64, which has three S buffers) and marks P V(g) done --
 // no P tile to wait for and no shared-memory fence before P V.
 // Every mbarrier wait is polled by the whole warp (one non-blocking probe, then a bounded loop):
 // a wait by one lane behind a branch costs several times more on this hardware.
@@ -44,11 +45,12 @@
 //
 // Differences from the page's kernel (made for this hardware):
 //  * the mask row is compacted once per item, so masked K/V tiles are never addressed;
-//  * S and P are double-buffered and a K stage is released as soon as its Q K^T is done (at
-//    d = 128 the commit that completes S[g & 1] frees K stage g % 2, and P V frees V stage g % 2;
-//    deeper rings have their own release barriers), so Q K^T of the
-//    next blocks runs while the softmax works, and the softmax of block g+1 runs while P V of
-//    block g is in the tensor pipe; the next item's loads overlap the current item's work;
+//  * S and P are double- or triple-buffered and a K stage is released as soon as its Q K^T is
+//    done (where a ring is as deep as the S buffers, the commits that complete S and free the S
+//    buffer also free its K and V stages; the third K stage at d = 128 has its own barrier), so
+//    Q K^T of the next blocks runs while the softmax works, and the softmax of block g+1 runs
+//    while P V of block g is in the tensor pipe; the next item's loads overlap the current
+//    item's work;
 //  * O lives in TMEM and is rescaled only when a row maximum grows by more than 2^8
 //    (exact: the final normaliser l is accumulated against the same reference maximum).
 // Every wait is bounded: on expiry the CTA records BSATTN_ERR_TIMEOUT, drains the copies and

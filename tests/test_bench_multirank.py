@@ -62,17 +62,18 @@ def test_reference_arm_runs_on_rank_zero_only():
 
 
 def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
-    """bench.py reports ncu DRAM traffic only while the hash of the kernel's sources (the .cu file
-    and the inline PTX helpers it includes) matches the one recorded with the counters, and only
-    for the workload the counters were taken on."""
+    """bench.py reports ncu DRAM traffic only while the hash of the kernel's code (the .cu file
+    and the inline PTX helpers it includes, comments and layout left out) matches the one recorded
+    with the counters, and only for the workload the counters were taken on."""
     import hashlib
     sys.path.insert(0, ROOT)
     import bench
     csrc = tmp_path / "block_sparse_attention_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    (csrc / "k.cu").write_bytes(b"kernel source\n")
-    (csrc / "h.cuh").write_bytes(b"helpers\n")
-    digest = hashlib.sha256(b"kernel source\nhelpers\n").hexdigest()[:16]
+    (csrc / "k.cu").write_text("int kernel = 1;  // a comment\n")
+    (csrc / "h.cuh").write_text("/* helpers */\nint helper = 2;\n")
+    digest = hashlib.sha256(b"int kernel = 1;\nint helper = 2;\n").hexdigest()[:16]
+    assert bench.source_digest([csrc / "k.cu", csrc / "h.cuh"]) == digest
     prof = tmp_path / "profiles"
     prof.mkdir()
     rec = {"k": {"source": ["k.cu", "h.cuh"], "source_sha256_16": digest, "bytes_per_launch": 1234,
@@ -82,5 +83,8 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("k", "C3") == 1234
     assert bench.traffic_record("k", "C2") is None          # taken on another workload
     assert bench.traffic_record("missing", "C3") is None
-    (csrc / "h.cuh").write_bytes(b"helpers, changed\n")
+    # a comment or layout edit keeps the record, a code edit drops it
+    (csrc / "k.cu").write_text("// reworded\n    int kernel = 1;   // another comment\n\n")
+    assert bench.traffic_record("k", "C3") == 1234
+    (csrc / "h.cuh").write_text("/* helpers */\nint helper = 3;\n")
     assert bench.traffic_record("k", "C3") is None
