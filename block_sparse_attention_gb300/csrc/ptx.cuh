@@ -100,7 +100,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Every lane of the warp waits (a converged poll is far cheaper than one lane waiting behind a
-// branch), then the warp agrees on the verdict.
+// branch), then the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait_parity(uint64_t* bar, uint32_t parity,
                                                  uint64_t deadline_ns, volatile int* abort_flag,
                                                  int* status) {
