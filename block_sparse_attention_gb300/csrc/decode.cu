@@ -802,3 +802,18 @@ extern "C" int bsattn_decode_varlen_noalloc(const void* q, const void* k, const 
     return bsattn_decode_varlen(q, k, v, cache_seqlens, block_indices, ns, out, B, Hq, Hkv, Smax,
                                 d, max_sel, dtype, scratch, kNoAllocScratchBytes, stream);
 }
+
+// The status word of the allocation-free decode sits at the start of the scratch array, where
+// the workspace of the other decode entry points keeps its own: read and cleared the same way,
+// after synchronising the stream (a 4-byte copy to a host word; nothing is allocated).
+extern "C" int bsattn_decode_noalloc_status(void* stream) {
+    using namespace bsattn;
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return BSATTN_ERR_CUDA;
+    if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return BSATTN_ERR_CUDA;
+    if (sdev != cur) return BSATTN_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    return bsattn_get_device_status(scratch, stream);
+}

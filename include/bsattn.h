@@ -152,12 +152,22 @@ int bsattn_decode_varlen(const void* q, const void* k, const void* v,
  * word and merge tickets with cudaMemsetAsync on `stream`.  All calls share the array, so
  * calls that overlap on the GPU (different streams, or threads) race and must be serialised
  * by the caller.  Device-detected conditions (a skipped out-of-range index, an expired
- * wait) are not reported by this variant.
+ * wait) go to the array's status word: read them with bsattn_decode_noalloc_status.
  */
 int bsattn_decode_varlen_noalloc(const void* q, const void* k, const void* v,
                                  const int32_t* cache_seqlens, const int32_t* block_indices,
                                  int num_splits, void* out, int B, int Hq, int Hkv, int Smax,
                                  int d, int max_sel, bsattn_dtype dtype, void* stream);
+
+/*
+ * Reads and clears the device status word of bsattn_decode_varlen_noalloc on the current
+ * device, after synchronising `stream` (which must belong to that device, else
+ * BSATTN_ERR_INVALID_ARG).  Each allocation-free call clears the word when it starts, so the
+ * result is the OR of the BSATTN_ERR_* bits (BSATTN_ERR_BAD_INDEX, BSATTN_ERR_TIMEOUT) that
+ * the most recent call recorded (0 = none), or BSATTN_ERR_CUDA if the read itself failed.
+ * It allocates nothing: a 4-byte copy into a host word.
+ */
+int bsattn_decode_noalloc_status(void* stream);
 
 /*
  * GQA varlen sparse decode, block-mask form -- [BSA] 6 (the `_mask` example).  Identical to

@@ -47,3 +47,55 @@ def test_noalloc_decode_matches_decode_and_oracle_twice(d, dtype, ns):
         assert float((out.float() - want.float()).abs().max()) <= TOL[dtype]
         err = float(np.abs(out.cpu().double().numpy() - oracle_out).max())
         assert err <= TOL[dtype], err
+
+
+def test_noalloc_status_reports_bad_index_and_expired_wait():
+    """Device-detected conditions of the allocation-free decode land in its array's status word,
+    read and cleared with bsattn_decode_noalloc_status: an index past the sequence end is skipped
+    and sets BSATTN_ERR_BAD_INDEX (the output still matches the oracle), a wait budget of 0 sets
+    BSATTN_ERR_TIMEOUT, and a clean call reports nothing."""
+    import block_sparse_attention_gb300 as bsa
+    lib = bsa.load()
+    f = lib.bsattn_decode_varlen_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, P]
+    f.restype = I
+    status = lib.bsattn_decode_noalloc_status
+    status.argtypes = [P]
+    status.restype = I
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, Hq, Hkv, Smax, nsel, d, dtype = 4, 16, 4, 4096, 16, 128, torch.bfloat16
+    sl, idx = synthetic.decode_selection(B, Hkv, 1000, Smax, nsel, nsel, seed=5)
+    q, k, v = synthetic.decode_qkv(B, Hq, Hkv, Smax, d, dtype, sl, seed=5)
+    bad = idx.clone()
+    bad[0, 0, 0] = (int(sl[0]) + 63) // 64          # the first block wholly past sequence 0's end
+    qd, kd, vd, sld = (t.to(dev) for t in (q, k, v, sl))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def call(index):
+        out = torch.full_like(qd, float("nan"))
+        rc = f(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), sld.data_ptr(), index.data_ptr(), 4,
+               out.data_ptr(), B, Hq, Hkv, Smax, d, nsel, 1, stream)
+        assert rc == 0, bsa.bsattn_status_string(rc)
+        return out
+
+    idxd, badd = idx.to(dev), bad.to(dev)
+    call(idxd)
+    assert status(stream) == 0
+    got = call(badd)
+    assert status(stream) & bsa.BSATTN_ERR_BAD_INDEX
+    assert status(stream) == 0                      # the read cleared it
+    err = float(np.abs(got.cpu().double().numpy() - oracle.decode_varlen(q, k, v, sl, bad)).max())
+    assert err <= TOL[dtype], err
+    try:
+        bsa.bsattn_set_wait_budget_ns(0)
+        call(idxd)
+        torch.cuda.synchronize()
+    finally:
+        bsa.bsattn_set_wait_budget_ns(2_000_000_000)
+    assert status(stream) & bsa.BSATTN_ERR_TIMEOUT
+    got = call(idxd)
+    assert status(stream) == 0
+    err = float(np.abs(got.cpu().double().numpy() - oracle.decode_varlen(q, k, v, sl, idx)).max())
+    assert err <= TOL[dtype], err
