@@ -30,6 +30,7 @@ __all__ = [
     "bsattn_mask_from_topk", "bsattn_mask_from_threshold", "bsattn_get_device_status",
     "bsattn_set_wait_budget_ns", "bsattn_status_string", "bsattn_version", "workspace",
     "bsattn_decode_varlen_mask", "bsattn_decode_paged", "bsattn_mask_from_cumulative_threshold",
+    "bsattn_decode_varlen_noalloc", "bsattn_decode_noalloc_status",
 ]
 
 BSATTN_OK = 0
@@ -83,6 +84,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 "bsattn_decode_paged": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, I, P, Z, P], I),
                 "bsattn_mask_from_cumulative_threshold": ([P, I, I, I, I, ctypes.c_double, I, P], I),
                 "bsattn_set_wait_budget_ns": ([ctypes.c_ulonglong], None),
+                "bsattn_decode_varlen_noalloc": ([P, P, P, P, P, I, P, I, I, I, I, I, I, I, P], I),
+                "bsattn_decode_noalloc_status": ([P], I),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -215,6 +218,37 @@ def bsattn_decode_varlen(q, k, v, cache_seqlens, block_indices, num_splits: int 
                                   _dtype_code(q), ws.data_ptr(), ws.numel(), _stream(q.device))
     _check("bsattn_decode_varlen", rc)
     return out
+
+
+def bsattn_decode_varlen_noalloc(q, k, v, cache_seqlens, block_indices, num_splits: int = 0, out=None):
+    """bsattn_decode_varlen on the library's own fixed scratch array (no workspace argument, no
+    device allocation by the library; `out` is allocated here when not given)."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("cache_seqlens", cache_seqlens),
+                    ("block_indices", block_indices)):
+        _cuda_contig(name, t)
+    if cache_seqlens.dtype != torch.int32 or block_indices.dtype != torch.int32:
+        raise TypeError("cache_seqlens and block_indices must be int32")
+    B, Hq, d = q.shape
+    _, Smax, Hkv, _ = k.shape
+    max_sel = block_indices.shape[2]
+    if tuple(block_indices.shape[:2]) != (B, Hkv) or k.shape != v.shape:
+        raise ValueError("decode shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.bsattn_decode_varlen_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          cache_seqlens.data_ptr(), block_indices.data_ptr(),
+                                          int(num_splits), out.data_ptr(), B, Hq, Hkv, Smax, d,
+                                          max_sel, _dtype_code(q), _stream(q.device))
+    _check("bsattn_decode_varlen_noalloc", rc)
+    return out
+
+
+def bsattn_decode_noalloc_status(device=None) -> int:
+    """Reads and clears the status word of the allocation-free decode on `device` (default: the
+    current one); syncs that device's current stream."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return int(load().bsattn_decode_noalloc_status(_stream(dev)))
 
 
 def bsattn_decode_varlen_mask(q, k, v, cache_seqlens, block_mask, num_splits: int = 0, out=None,

@@ -47,6 +47,10 @@ def test_noalloc_decode_matches_decode_and_oracle_twice(d, dtype, ns):
         assert float((out.float() - want.float()).abs().max()) <= TOL[dtype]
         err = float(np.abs(out.cpu().double().numpy() - oracle_out).max())
         assert err <= TOL[dtype], err
+    # the same call through the Python binding
+    out = bsa.bsattn_decode_varlen_noalloc(qd, kd, vd, sld, idxd, ns)
+    assert bsa.bsattn_decode_noalloc_status() == 0
+    assert float((out.float() - want.float()).abs().max()) <= TOL[dtype]
 
 
 def test_noalloc_status_reports_bad_index_and_expired_wait():
